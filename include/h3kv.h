@@ -1,0 +1,127 @@
+/*
+ * h3kv.h -- C ABI of libh3kv: the kvi8r rotated-int8 whole-sequence K/V store
+ * and query-chunked attention over it, on one NVIDIA GB300 (sm_103a).
+ *
+ * Source of the method: "H3 Streamed Blocks (exact low-VRAM, alpha)", Inputs
+ * table (kv_store, q_chunk, kv_block rows), and "Low VRAM, low RAM: the
+ * de-rope on a 16 GB card", section "The K/V store options" (kvi8r row and the
+ * paragraph on why the rotation).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Layout: every tensor is contiguous, head-major [heads, seq, head_dim]
+ *    with head_dim == 128; per-row scales are [heads, seq].  bf16 and fp16
+ *    values are passed as their 16-bit patterns (uint16_t).
+ *  - Memory: all tensor pointers are DEVICE pointers on the current CUDA
+ *    device, 16-byte aligned, owned by the caller.  The library allocates no
+ *    device memory and frees nothing.
+ *  - Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *    Calls are stream-ordered and asynchronous: they return after the launch.
+ *  - Errors: argument checks run on the host before any launch and return
+ *    H3KV_ERR_INVALID_ARG / H3KV_ERR_UNSUPPORTED with nothing launched.  A
+ *    launch failure returns H3KV_ERR_CUDA.  Every wait inside the kernels is
+ *    bounded; a wait that runs out records a device error word and the kernel
+ *    returns early.  h3kv_sync_status() reports (and clears) that word.
+ *  - Empty work (heads == 0 or a zero sequence length) returns H3KV_OK and
+ *    launches nothing, except that attending a non-empty query set to an
+ *    empty key set is H3KV_ERR_INVALID_ARG (the softmax has no terms).
+ */
+#ifndef H3KV_H
+#define H3KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define H3KV_ABI_VERSION 1u
+#define H3KV_HEAD_DIM 128
+/* kv_block = 0 on the kvi8r path means this many tokens (the kv_block
+ * default of the kv_store row). */
+#define H3KV_DEFAULT_KV_BLOCK 16384
+/* kv_block must be 0 or a multiple of this (the key tile of the kernels). */
+#define H3KV_KV_TILE 128
+
+typedef enum {
+  H3KV_OK = 0,
+  H3KV_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad size or chunk  */
+  H3KV_ERR_UNSUPPORTED = 2,    /* head_dim != 128, or device is not sm_103   */
+  H3KV_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed       */
+  H3KV_ERR_DEVICE_TIMEOUT = 4  /* a bounded in-kernel wait ran out           */
+} h3kv_status;
+
+/* The kvi8r store: for K and for V, int8 codes [heads, seq, 128] and one fp16
+ * scale per (head, token) row [heads, seq].  The codes are the rows of K (or
+ * V) rotated into the orthonormal Sylvester-Hadamard basis H (x' = x H, H the
+ * order-128 Hadamard matrix / sqrt(128)), quantised as
+ *   s = fp16_rne(max_j |x'_j| / 127)   (saturated at 65504),
+ *   c_j = clamp(rne(x'_j / s), -127, 127),   c = 0 where s == 0.
+ * Dequantisation is c * s.  All four buffers are caller-owned device memory. */
+typedef struct {
+  int8_t *k_codes;
+  int8_t *v_codes;
+  uint16_t *k_scales; /* fp16 bit patterns */
+  uint16_t *v_scales; /* fp16 bit patterns */
+  int32_t heads;
+  int64_t seq;
+  int32_t head_dim; /* must be 128 */
+} h3kv_store;
+
+/* Version of this ABI (H3KV_ABI_VERSION). */
+uint32_t h3kv_abi_version(void);
+
+/* Bytes of device memory a store of this shape occupies in total (codes and
+ * scales of K and V): 2 * heads * seq * (head_dim + 2).  Returns 0 for
+ * invalid shapes. */
+size_t h3kv_store_bytes(int32_t heads, int64_t seq, int32_t head_dim);
+
+/* Build the kvi8r store from bf16 K and V [heads, seq, 128] (kv_store row of
+ * the H3 Streamed Blocks Inputs table: rotate by the fixed Hadamard basis,
+ * one fp16 absmax scale per token per head, int8 codes).  `out` describes the
+ * destination buffers and must match heads/seq/head_dim.  K and V are read
+ * once; codes and scales are written once. */
+h3kv_status h3kv_build_store(const uint16_t *K, const uint16_t *V, int32_t heads, int64_t seq,
+                             int32_t head_dim, const h3kv_store *out, void *stream);
+
+/* kvi8r attention (kv_store row): O = softmax(q' K'^T * softmax_scale) V' H^T
+ * where q' = Q H rounded to fp16, K' and V' are the dequantised store
+ * (int8 -> fp16 cast times the fp16 scale), the softmax runs over all
+ * store->seq keys (non-causal), in kv_block-token blocks combined by their
+ * log-sum-exp, and the output is un-rotated once.
+ *   Q: bf16 [store->heads, q_seq, 128].  O: fp32 [store->heads, q_seq, 128].
+ *   q_chunk >= 1: query tokens per kernel launch (the q_chunk input).  The
+ *     output is bit-identical for every q_chunk ("exact at any value").
+ *   kv_block: 0 (= 16384) or a positive multiple of 128.
+ *   softmax_scale <= 0 selects 1/sqrt(128). */
+h3kv_status h3kv_attend(const uint16_t *Q, int64_t q_seq, const h3kv_store *store, int32_t q_chunk,
+                        int32_t kv_block, float softmax_scale, float *O, void *stream);
+
+/* The exact store (the "bf16 (exact)" kv_store option): plain softmax
+ * attention on bf16 K and V, O = softmax(Q K^T * softmax_scale) V, with P
+ * rounded to bf16 for the second product and fp32 accumulation.
+ *   Q: bf16 [heads, q_seq, 128]; K, V: bf16 [heads, kv_seq, 128];
+ *   O: fp32 [heads, q_seq, 128].
+ *   q_chunk >= 1 as above (bit-identical for every value).
+ *   kv_block: 0 (= one block over all keys) or a positive multiple of 128:
+ *     keys are attended in blocks combined by their log-sum-exp (the kv_block
+ *     input).
+ *   softmax_scale <= 0 selects 1/sqrt(128). */
+h3kv_status h3kv_attend_exact(const uint16_t *Q, int64_t q_seq, const uint16_t *K, const uint16_t *V,
+                              int32_t heads, int64_t kv_seq, int32_t head_dim, int32_t q_chunk,
+                              int32_t kv_block, float softmax_scale, float *O, void *stream);
+
+/* Synchronise `stream`, then return and clear the device error word that the
+ * kernels set when a bounded wait runs out (H3KV_ERR_DEVICE_TIMEOUT), or
+ * H3KV_ERR_CUDA if the synchronisation itself reports an error. */
+h3kv_status h3kv_sync_status(void *stream);
+
+/* Static description of a status code (never NULL). */
+const char *h3kv_strerror(h3kv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* H3KV_H */

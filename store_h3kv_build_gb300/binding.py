@@ -1,0 +1,142 @@
+"""Thin Python binding over ``libh3kv.so`` (the C ABI in ``include/h3kv.h``).
+
+Argument marshalling only: torch tensors are used for device memory and the
+current CUDA stream, their pointers and sizes go through ctypes, and every
+step of the computation runs in the library's CUDA kernels.  Importing this
+module loads the library and raises ImportError if it has not been built
+(``python -m store_h3kv_build_gb300.build_lib``); there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libh3kv.so")
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m store_h3kv_build_gb300.build_lib`")
+_lib = ctypes.CDLL(LIB_PATH)
+
+HEAD_DIM = 128
+DEFAULT_KV_BLOCK = 16384
+KV_TILE = 128
+
+H3KV_OK = 0
+H3KV_ERR_INVALID_ARG = 1
+H3KV_ERR_UNSUPPORTED = 2
+H3KV_ERR_CUDA = 3
+H3KV_ERR_DEVICE_TIMEOUT = 4
+
+
+class h3kv_store(ctypes.Structure):  # noqa: N801 - mirrors the C struct name
+    _fields_ = [
+        ("k_codes", ctypes.c_void_p),
+        ("v_codes", ctypes.c_void_p),
+        ("k_scales", ctypes.c_void_p),
+        ("v_scales", ctypes.c_void_p),
+        ("heads", ctypes.c_int32),
+        ("seq", ctypes.c_int64),
+        ("head_dim", ctypes.c_int32),
+    ]
+
+
+_vp, _i32, _i64, _f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+_SIGS = {
+    "h3kv_abi_version": (ctypes.c_uint32, []),
+    "h3kv_store_bytes": (ctypes.c_size_t, [_i32, _i64, _i32]),
+    "h3kv_build_store": (ctypes.c_int, [_vp, _vp, _i32, _i64, _i32, ctypes.POINTER(h3kv_store), _vp]),
+    "h3kv_attend": (ctypes.c_int, [_vp, _i64, ctypes.POINTER(h3kv_store), _i32, _i32, _f32, _vp, _vp]),
+    "h3kv_attend_exact": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _f32, _vp, _vp]),
+    "h3kv_sync_status": (ctypes.c_int, [_vp]),
+    "h3kv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+    globals()[_name] = _fn
+
+EXPORTED = tuple(_SIGS)
+
+
+class H3kvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {h3kv_strerror(status).decode()} (status {status})")
+
+
+def check(status: int, where: str = "h3kv") -> None:
+    if status != H3KV_OK:
+        raise H3kvError(status, where)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+class Store:
+    """A kvi8r store held in torch tensors: int8 codes [heads, seq, 128] and
+    fp16 scales [heads, seq] for K and for V."""
+
+    def __init__(self, k_codes, v_codes, k_scales, v_scales):
+        self.k_codes, self.v_codes = k_codes, v_codes
+        self.k_scales, self.v_scales = k_scales, v_scales
+        self.heads, self.seq = int(k_codes.shape[0]), int(k_codes.shape[1])
+
+    @classmethod
+    def empty(cls, heads: int, seq: int, device="cuda") -> "Store":
+        kc = torch.empty((heads, seq, HEAD_DIM), dtype=torch.int8, device=device)
+        vc = torch.empty_like(kc)
+        ks = torch.empty((heads, seq), dtype=torch.float16, device=device)
+        vs = torch.empty_like(ks)
+        return cls(kc, vc, ks, vs)
+
+    def c_struct(self) -> h3kv_store:
+        return h3kv_store(_ptr(self.k_codes), _ptr(self.v_codes), _ptr(self.k_scales), _ptr(self.v_scales),
+                          self.heads, self.seq, HEAD_DIM)
+
+    def nbytes(self) -> int:
+        return int(h3kv_store_bytes(self.heads, self.seq, HEAD_DIM))
+
+
+def build_store(K: torch.Tensor, V: torch.Tensor, out: Store | None = None, stream=None) -> Store:
+    """h3kv_build_store on bf16 K, V [heads, seq, 128] (CUDA, contiguous)."""
+    heads, seq = int(K.shape[0]), int(K.shape[1])
+    out = Store.empty(heads, seq, K.device) if out is None else out
+    st = out.c_struct()
+    check(h3kv_build_store(_ptr(K), _ptr(V), heads, seq, int(K.shape[2]), ctypes.byref(st), _stream(stream)),
+          "h3kv_build_store")
+    return out
+
+
+def attend(Q: torch.Tensor, store: Store, q_chunk: int = 16384, kv_block: int = 0, softmax_scale: float = 0.0,
+           out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """h3kv_attend: kvi8r attention of bf16 Q [heads, q_seq, 128] over `store`
+    -> fp32 [heads, q_seq, 128]."""
+    q_seq = int(Q.shape[1])
+    out = torch.empty(Q.shape, dtype=torch.float32, device=Q.device) if out is None else out
+    st = store.c_struct()
+    check(h3kv_attend(_ptr(Q), q_seq, ctypes.byref(st), int(q_chunk), int(kv_block), float(softmax_scale),
+                      _ptr(out), _stream(stream)), "h3kv_attend")
+    return out
+
+
+def attend_exact(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, q_chunk: int = 16384, kv_block: int = 0,
+                 softmax_scale: float = 0.0, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """h3kv_attend_exact: softmax attention on bf16 Q, K, V -> fp32."""
+    out = torch.empty(Q.shape, dtype=torch.float32, device=Q.device) if out is None else out
+    check(h3kv_attend_exact(_ptr(Q), int(Q.shape[1]), _ptr(K), _ptr(V), int(K.shape[0]), int(K.shape[1]),
+                            int(K.shape[2]), int(q_chunk), int(kv_block), float(softmax_scale), _ptr(out),
+                            _stream(stream)), "h3kv_attend_exact")
+    return out
+
+
+def sync_status(stream=None) -> None:
+    """Synchronise the stream and raise if a kernel recorded a wait timeout."""
+    check(h3kv_sync_status(_stream(stream)), "h3kv_sync_status")

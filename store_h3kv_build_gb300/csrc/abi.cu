@@ -1,0 +1,252 @@
+// abi.cu -- the C ABI of libh3kv (declared in include/h3kv.h): host-side
+// argument checks, TMA tensor-map encoding, per-chunk launches and the device
+// error word.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <mutex>
+
+#include "../../include/h3kv.h"
+#include "kernels.h"
+
+namespace {
+
+// Device error word written by the kernels' bounded waits.  Host code must
+// not take its address directly (that is a host shadow); the device address is
+// fetched per device with cudaGetSymbolAddress.
+__device__ uint32_t g_h3kv_error;
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s per bounded wait
+
+struct DeviceInfo {
+  bool ready = false;
+  bool supported = false;
+  int num_sms = 0;
+  uint32_t *err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+h3kv_status device_info(DeviceInfo **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return H3KV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo &d = g_dev[dev];
+  if (!d.ready) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return H3KV_ERR_CUDA;
+    d.supported = (prop.major == 10 && prop.minor == 3);
+    d.num_sms = prop.multiProcessorCount;
+    if (d.supported) {
+      void *p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_h3kv_error) != cudaSuccess) return H3KV_ERR_CUDA;
+      d.err = static_cast<uint32_t *>(p);
+      if (cudaMemset(d.err, 0, sizeof(uint32_t)) != cudaSuccess) return H3KV_ERR_CUDA;
+      if (cudaDeviceSynchronize() != cudaSuccess) return H3KV_ERR_CUDA;
+    }
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void *fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return H3KV_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.ready = true;
+  }
+  if (!d.supported) return H3KV_ERR_UNSUPPORTED;
+  *out = &d;
+  return H3KV_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 2-D map over a row-major [rows, 128] matrix of 1- or 2-byte elements.
+bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t rows, uint32_t elem_bytes,
+               uint32_t box_inner) {
+  const cuuint64_t dims[2] = {128, rows};
+  const cuuint64_t strides[1] = {128ull * elem_bytes};
+  const cuuint32_t box[2] = {box_inner, 128};
+  const cuuint32_t es[2] = {1, 1};
+  return g_encode(m, dt, 2, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map over bf16 [heads, seq, 128]: box 64 x 128 rows x 1 head; rows past
+// `seq` read as zero.
+bool encode_3d_bf16(CUtensorMap *m, const void *base, uint64_t seq, uint64_t heads) {
+  const cuuint64_t dims[3] = {128, seq, heads};
+  const cuuint64_t strides[2] = {256, seq * 256};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// TMA coordinates are signed 32-bit; keep every row index below 2^31.
+constexpr int64_t kMaxRows = (1ll << 31) - 256;
+
+h3kv_status check_chunks(int32_t q_chunk, int32_t kv_block) {
+  if (q_chunk < 1) return H3KV_ERR_INVALID_ARG;
+  if (kv_block < 0 || kv_block % H3KV_KV_TILE != 0) return H3KV_ERR_INVALID_ARG;
+  return H3KV_OK;
+}
+
+float scale_log2_of(float softmax_scale) {
+  const float s = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(128.0f);
+  return s * 1.4426950408889634f;
+}
+
+}  // namespace
+
+extern "C" {
+
+uint32_t h3kv_abi_version(void) { return H3KV_ABI_VERSION; }
+
+size_t h3kv_store_bytes(int32_t heads, int64_t seq, int32_t head_dim) {
+  if (heads < 0 || seq < 0 || head_dim != H3KV_HEAD_DIM) return 0;
+  return static_cast<size_t>(2) * static_cast<size_t>(heads) * static_cast<size_t>(seq) *
+         static_cast<size_t>(head_dim + 2);
+}
+
+const char *h3kv_strerror(h3kv_status status) {
+  switch (status) {
+    case H3KV_OK: return "ok";
+    case H3KV_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad size, q_chunk or kv_block)";
+    case H3KV_ERR_UNSUPPORTED: return "unsupported (head_dim must be 128; device must be sm_103)";
+    case H3KV_ERR_CUDA: return "CUDA runtime error";
+    case H3KV_ERR_DEVICE_TIMEOUT: return "a bounded in-kernel wait ran out";
+  }
+  return "unknown status";
+}
+
+h3kv_status h3kv_build_store(const uint16_t *K, const uint16_t *V, int32_t heads, int64_t seq, int32_t head_dim,
+                             const h3kv_store *out, void *stream) {
+  if (heads < 0 || seq < 0 || !out) return H3KV_ERR_INVALID_ARG;
+  if (head_dim != H3KV_HEAD_DIM || out->head_dim != H3KV_HEAD_DIM) return H3KV_ERR_UNSUPPORTED;
+  if (out->heads != heads || out->seq != seq) return H3KV_ERR_INVALID_ARG;
+  const int64_t rows = static_cast<int64_t>(heads) * seq;
+  if (rows == 0) return H3KV_OK;
+  if (rows > kMaxRows) return H3KV_ERR_INVALID_ARG;
+  if (!K || !V || !out->k_codes || !out->v_codes || !out->k_scales || !out->v_scales) return H3KV_ERR_INVALID_ARG;
+  if (!aligned16(K) || !aligned16(V) || !aligned16(out->k_codes) || !aligned16(out->v_codes) ||
+      !aligned16(out->k_scales) || !aligned16(out->v_scales))
+    return H3KV_ERR_INVALID_ARG;
+  DeviceInfo *d = nullptr;
+  h3kv_status st = device_info(&d);
+  if (st != H3KV_OK) return st;
+  CUtensorMap k_in, v_in, k_out, v_out;
+  if (!encode_2d(&k_in, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, rows, 2, 64) ||
+      !encode_2d(&v_in, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, 2, 64) ||
+      !encode_2d(&k_out, CU_TENSOR_MAP_DATA_TYPE_UINT8, out->k_codes, rows, 1, 128) ||
+      !encode_2d(&v_out, CU_TENSOR_MAP_DATA_TYPE_UINT8, out->v_codes, rows, 1, 128))
+    return H3KV_ERR_CUDA;
+  const cudaError_t e = h3kv::launch_store_build(k_in, v_in, k_out, v_out, out->k_scales, out->v_scales, rows,
+                                                 d->num_sms, d->err, kDefaultTimeoutNs,
+                                                 static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? H3KV_OK : H3KV_ERR_CUDA;
+}
+
+h3kv_status h3kv_attend(const uint16_t *Q, int64_t q_seq, const h3kv_store *store, int32_t q_chunk,
+                        int32_t kv_block, float softmax_scale, float *O, void *stream) {
+  if (!store || q_seq < 0 || store->heads < 0 || store->seq < 0) return H3KV_ERR_INVALID_ARG;
+  if (store->head_dim != H3KV_HEAD_DIM) return H3KV_ERR_UNSUPPORTED;
+  h3kv_status st = check_chunks(q_chunk, kv_block);
+  if (st != H3KV_OK) return st;
+  if (store->heads == 0 || q_seq == 0) return H3KV_OK;
+  if (store->seq == 0) return H3KV_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(store->heads) * q_seq > kMaxRows || static_cast<int64_t>(store->heads) * store->seq > kMaxRows)
+    return H3KV_ERR_INVALID_ARG;
+  if (!Q || !O || !store->k_codes || !store->v_codes || !store->k_scales || !store->v_scales)
+    return H3KV_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(O) || !aligned16(store->k_codes) || !aligned16(store->v_codes) ||
+      !aligned16(store->k_scales) || !aligned16(store->v_scales))
+    return H3KV_ERR_INVALID_ARG;
+  DeviceInfo *d = nullptr;
+  st = device_info(&d);
+  if (st != H3KV_OK) return st;
+  const int32_t kvb = kv_block == 0 ? H3KV_DEFAULT_KV_BLOCK : kv_block;
+  h3kv::AttnArgs a{};
+  a.q = Q;
+  a.k_codes = store->k_codes;
+  a.v_codes = store->v_codes;
+  a.k_scales = store->k_scales;
+  a.v_scales = store->v_scales;
+  a.o = O;
+  a.q_seq = q_seq;
+  a.kv_seq = store->seq;
+  a.heads = store->heads;
+  a.kv_block_tiles = kvb / H3KV_KV_TILE;
+  a.scale_log2 = scale_log2_of(softmax_scale);
+  a.err = d->err;
+  a.timeout_ns = kDefaultTimeoutNs;
+  for (int64_t c0 = 0; c0 < q_seq; c0 += q_chunk) {
+    a.q_begin = c0;
+    a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
+    if (h3kv::launch_attend_kvi8r(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return H3KV_ERR_CUDA;
+  }
+  return H3KV_OK;
+}
+
+h3kv_status h3kv_attend_exact(const uint16_t *Q, int64_t q_seq, const uint16_t *K, const uint16_t *V,
+                              int32_t heads, int64_t kv_seq, int32_t head_dim, int32_t q_chunk, int32_t kv_block,
+                              float softmax_scale, float *O, void *stream) {
+  if (q_seq < 0 || heads < 0 || kv_seq < 0) return H3KV_ERR_INVALID_ARG;
+  if (head_dim != H3KV_HEAD_DIM) return H3KV_ERR_UNSUPPORTED;
+  h3kv_status st = check_chunks(q_chunk, kv_block);
+  if (st != H3KV_OK) return st;
+  if (heads == 0 || q_seq == 0) return H3KV_OK;
+  if (kv_seq == 0) return H3KV_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(heads) * q_seq > kMaxRows || static_cast<int64_t>(heads) * kv_seq > kMaxRows)
+    return H3KV_ERR_INVALID_ARG;
+  if (!Q || !K || !V || !O) return H3KV_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return H3KV_ERR_INVALID_ARG;
+  DeviceInfo *d = nullptr;
+  st = device_info(&d);
+  if (st != H3KV_OK) return st;
+  CUtensorMap tq, tk, tv;
+  if (!encode_3d_bf16(&tq, Q, static_cast<uint64_t>(q_seq), static_cast<uint64_t>(heads)) ||
+      !encode_3d_bf16(&tk, K, static_cast<uint64_t>(kv_seq), static_cast<uint64_t>(heads)) ||
+      !encode_3d_bf16(&tv, V, static_cast<uint64_t>(kv_seq), static_cast<uint64_t>(heads)))
+    return H3KV_ERR_CUDA;
+  const int64_t n_tiles = (kv_seq + H3KV_KV_TILE - 1) / H3KV_KV_TILE;
+  h3kv::AttnArgs a{};
+  a.q = Q;
+  a.o = O;
+  a.q_seq = q_seq;
+  a.kv_seq = kv_seq;
+  a.heads = heads;
+  a.kv_block_tiles = kv_block == 0 ? static_cast<int32_t>(n_tiles) : kv_block / H3KV_KV_TILE;
+  a.scale_log2 = scale_log2_of(softmax_scale);
+  a.err = d->err;
+  a.timeout_ns = kDefaultTimeoutNs;
+  for (int64_t c0 = 0; c0 < q_seq; c0 += q_chunk) {
+    a.q_begin = c0;
+    a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
+    if (h3kv::launch_attend_exact(tq, tk, tv, a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return H3KV_ERR_CUDA;
+  }
+  return H3KV_OK;
+}
+
+h3kv_status h3kv_sync_status(void *stream) {
+  DeviceInfo *d = nullptr;
+  h3kv_status st = device_info(&d);
+  if (st != H3KV_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return H3KV_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, d->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return H3KV_ERR_CUDA;
+  if (word != 0) {
+    if (cudaMemset(d->err, 0, sizeof(uint32_t)) != cudaSuccess) return H3KV_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return H3KV_ERR_CUDA;
+    return H3KV_ERR_DEVICE_TIMEOUT;
+  }
+  return H3KV_OK;
+}
+
+}  // extern "C"

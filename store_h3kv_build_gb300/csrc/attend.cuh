@@ -1,0 +1,541 @@
+// attend.cuh -- query-chunked attention over a whole-sequence K/V store on
+// sm_103a tensor cores (tcgen05 + TMEM), shared by the kvi8r and the exact
+// (bf16) store.
+//
+// kvi8r (kv_store row of the H3 Streamed Blocks Inputs table; kvi8r row and
+// the rotation paragraph of "The K/V store options" in the Low VRAM
+// write-up): the query chunk is rotated into the Hadamard basis (q' = q H,
+// fp16), each K/V block is dequantised as int8 -> fp16 cast times the row
+// scale, scores and P.V run in fp16 with fp32 accumulation, blocks of
+// kv_block keys are combined by their log-sum-exp, and the output is
+// un-rotated once (O = O' H^T).  The exact store runs the same pipeline on
+// bf16 K/V without rotation or dequantisation.
+//
+// One CTA owns 256 query rows of one head (two 128-row tiles, so that the
+// softmax of one tile overlaps the tensor-core work of the other) and walks
+// every 128-key tile of that head in a fixed order, so a query row's
+// arithmetic never depends on q_chunk or on which CTA holds it.
+//
+// Warp roles (512 threads):
+//   warps 0-3   softmax / correction / epilogue of query tile 0 (thread = row)
+//   warps 4-7   the same for query tile 1
+//   warps 8-11  kvi8r: in-place int8 -> fp16 dequantisation of K and V tiles
+//   warp 12     producer: TMA / bulk copies of Q (exact) and K/V tiles
+//   warp 13     TMEM allocation and tcgen05.mma issue (one thread)
+//   warps 14-15 idle
+// TMEM (512 columns x 128 lanes, fp32): S0 [0,128), S1 [128,256) with P0/P1
+// (fp16/bf16 pairs) written over the first 64 columns of S0/S1, O0
+// [256,384), O1 [384,512).
+#pragma once
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace h3kv {
+namespace attn {
+
+constexpr int kBM = 128;                    // query rows per tile (MMA M)
+constexpr int kNQ = 2;                      // query tiles per CTA
+constexpr int kBN = 128;                    // keys per tile
+constexpr int kNK = 3;                      // K tile ring depth
+constexpr int kNV = 2;                      // V tile ring depth
+constexpr int kTileBytes = 128 * 128 * 2;   // one 16-bit [128 x 128] tile
+constexpr int kChunkBytes = kTileBytes / 2; // 64-column half (one swizzle atom wide)
+constexpr int kThreads = 512;
+constexpr float kLazyRescaleLog2 = 8.0f;    // rescale O only when the max grows by > 2^8
+
+// Register split per warpgroup (setmaxnreg).  The launch gives every thread
+// 128 (512 threads x 128 = the 64K register file); each split below sums to
+// the same total: 128 x (2 x softmax + dequant + issue) = 65536.
+constexpr uint32_t kRegSoftmax = 184;
+constexpr uint32_t kRegDequantKvi8r = 64, kRegIssueKvi8r = 80;
+constexpr uint32_t kRegDequantExact = 56, kRegIssueExact = 88;
+static_assert(2 * kRegSoftmax + kRegDequantKvi8r + kRegIssueKvi8r == 512, "register split");
+static_assert(2 * kRegSoftmax + kRegDequantExact + kRegIssueExact == 512, "register split");
+
+struct Smem {
+  uint8_t q[kNQ][kTileBytes];
+  uint8_t k[kNK][kTileBytes];
+  uint8_t v[kNV][kTileBytes];
+  uint64_t q_full;
+  uint64_t k_load[kNK], k_ready[kNK], k_free[kNK];
+  uint64_t v_load[kNV], v_ready[kNV], v_free[kNV];
+  uint64_t s_full[kNQ], p_full[kNQ];
+  uint64_t o_full;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx &w) {
+  const bool ok = mbar_wait(bar, parity, w);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// 16 int8 codes (one 16-byte granule) -> 16 fp16 values code * scale.  The
+// code is biased to an unsigned byte u = c + 128, placed in the mantissa of
+// the fp16 value 1024 + u by a byte permute, and 1152 is subtracted exactly,
+// giving fp16(c) exactly; the multiply by the fp16 scale rounds once.
+__device__ __forceinline__ void dequant16(const uint4 raw, const __half2 s2, uint32_t (&out)[8]) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));  // 1152
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t u = w[k] ^ 0x80808080u;
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
+    const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
+    const __half2 ha = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&a), bias), s2);
+    const __half2 hb = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&b), bias), s2);
+    out[2 * k] = *reinterpret_cast<const uint32_t *>(&ha);
+    out[2 * k + 1] = *reinterpret_cast<const uint32_t *>(&hb);
+  }
+}
+
+// In-place dequantisation of one K or V tile by the 128 dequant threads.
+// On entry the int8 codes of the tile's rows sit linearly (128 bytes per row)
+// in the second half of the tile buffer; on exit the whole buffer holds the
+// fp16 tile in the 128B-swizzled layout the MMA descriptors expect (two
+// 64-column halves of [128 rows x 128 bytes]).  Row r's codes share their
+// 128-byte slot with row r's fp16 columns 64-127, and each row is read by its
+// own 8 lanes in one instruction before they write it, so in place is safe.
+__device__ __forceinline__ void dequant_tile(uint8_t *tile, const uint16_t *scales, int valid, int dw, int lane) {
+  const uint32_t g = lane & 7;
+  uint16_t sc[8];
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int r = dw * 32 + it * 4 + (lane >> 3);
+    sc[it] = r < valid ? scales[r] : 0;
+  }
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const uint32_t r = dw * 32 + it * 4 + (lane >> 3);
+    const uint4 raw = *reinterpret_cast<const uint4 *>(tile + kChunkBytes + r * 128 + g * 16);
+    const __half s = __ushort_as_half(sc[it]);
+    uint32_t o[8];
+    dequant16(raw, __halves2half2(s, s), o);
+    uint8_t *half_base = tile + (g >> 2) * kChunkBytes;
+    const uint32_t G0 = (g & 3) * 2;
+    *reinterpret_cast<uint4 *>(half_base + sw128_off(r, G0)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4 *>(half_base + sw128_off(r, G0 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+template <bool kKvi8r>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (kKvi8r) return pack_f16x2(lo, hi);
+  else return pack_bf16x2(lo, hi);
+}
+
+template <bool kKvi8r>
+__global__ void __launch_bounds__(kThreads, 1)
+    attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int h = blockIdx.y;
+  const int64_t row0 = a.q_begin + static_cast<int64_t>(blockIdx.x) * (kNQ * kBM);
+  const int n_tiles = static_cast<int>((a.kv_seq + kBN - 1) / kBN);
+  const int blk = a.kv_block_tiles;
+
+  if (tid == 0) {
+    mbar_init(smem_u32(&sm.q_full), kKvi8r ? kNQ * kBM : 1);
+    for (int s = 0; s < kNK; ++s) {
+      mbar_init(smem_u32(&sm.k_load[s]), 1);
+      mbar_init(smem_u32(&sm.k_ready[s]), 128);
+      mbar_init(smem_u32(&sm.k_free[s]), 1);
+    }
+    for (int s = 0; s < kNV; ++s) {
+      mbar_init(smem_u32(&sm.v_load[s]), 1);
+      mbar_init(smem_u32(&sm.v_ready[s]), 128);
+      mbar_init(smem_u32(&sm.v_free[s]), 1);
+    }
+    for (int q = 0; q < kNQ; ++q) {
+      mbar_init(smem_u32(&sm.s_full[q]), 1);
+      mbar_init(smem_u32(&sm.p_full[q]), kBM);
+    }
+    mbar_init(smem_u32(&sm.o_full), 1);
+    mbar_init(smem_u32(&sm.drain), 1);
+    sm.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 13) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const WaitCtx wctx{a.err, &sm.abort, a.timeout_ns};
+
+  if (warp < 8) {
+    // =================================================== softmax warpgroups
+    reg_alloc<kRegSoftmax>();
+    const int q = warp >> 2;
+    const uint32_t i = tid & 127;  // row in the query tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + q * 128;
+    const uint32_t tO = tmem + lane_base + 256 + q * 128;
+    const int64_t row = row0 + q * kBM + i;
+    const bool row_ok = row < a.q_end;
+    float *orow = a.o + (static_cast<int64_t>(h) * a.q_seq + (row_ok ? row : 0)) * 128;
+    const float c2 = a.scale_log2;
+
+    if constexpr (kKvi8r) {
+      // q' = fp16(q H): each warp rotates its 32 rows of the query tile, one
+      // row at a time across the warp (lane l holds elements 4l..4l+3), and
+      // writes them in the 128B-swizzled K-major layout of the MMA's A operand.
+      const int wq = warp & 3;
+      uint2 buf[32];
+#pragma unroll
+      for (int rr = 0; rr < 32; ++rr) {
+        const int64_t r = row0 + q * kBM + wq * 32 + rr;
+        buf[rr] = r < a.q_end ? *reinterpret_cast<const uint2 *>(a.q + (static_cast<int64_t>(h) * a.q_seq + r) * 128 +
+                                                                  4 * lane)
+                              : make_uint2(0u, 0u);
+      }
+#pragma unroll
+      for (int rr = 0; rr < 32; ++rr) {
+        const uint32_t ti = wq * 32 + rr;
+        float x[4] = {bf16lo_to_f32(buf[rr].x), bf16hi_to_f32(buf[rr].x), bf16lo_to_f32(buf[rr].y),
+                      bf16hi_to_f32(buf[rr].y)};
+        fwht128_warp(x, lane);
+        const uint2 w = make_uint2(pack_f16x2(x[0] * kInvSqrt128, x[1] * kInvSqrt128),
+                                   pack_f16x2(x[2] * kInvSqrt128, x[3] * kInvSqrt128));
+        *reinterpret_cast<uint2 *>(sm.q[q] + (lane >> 4) * kChunkBytes + sw128_off(ti, (lane & 15) >> 1) +
+                                   (lane & 1) * 8) = w;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&sm.q_full));
+    }
+
+    float m_b = 0.f, l_b = 0.f;  // current block: running max (raw score units) and sum
+    float M = 0.f, Lam = 0.f;    // blocks merged so far
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      if (!warp_wait(smem_u32(&sm.s_full[q]), j & 1, wctx)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+      const int64_t valid = a.kv_seq - static_cast<int64_t>(j) * kBN;
+      if (valid < kBN) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) s[c] = (c < valid) ? s[c] : -INFINITY;
+      }
+      float mt = s[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mt = fmaxf(mt, s[c]);
+
+      if (j % blk == 0) {
+        if (j > 0) {
+          // merge the finished block (O_q, m_b, l_b) into (M, Lam, O row in
+          // global memory, rotated basis, un-normalised)
+          const bool first = (j / blk) == 1;
+          float al = 0.f, be = 1.f;
+          if (!first) {
+            const float Mn = fmaxf(M, m_b);
+            al = ex2((M - Mn) * c2);
+            be = ex2((m_b - Mn) * c2);
+            Lam = Lam * al + l_b * be;
+            M = Mn;
+          } else {
+            M = m_b;
+            Lam = l_b;
+          }
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {
+            float o[16];
+            tmem_ld16(tO + c * 16, *reinterpret_cast<uint32_t(*)[16]>(o));
+            if (row_ok) {
+              float4 *dst = reinterpret_cast<float4 *>(orow + c * 16);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                float4 v = make_float4(o[4 * k] * be, o[4 * k + 1] * be, o[4 * k + 2] * be, o[4 * k + 3] * be);
+                if (!first) {
+                  const float4 g = dst[k];
+                  v.x = fmaf(g.x, al, v.x);
+                  v.y = fmaf(g.y, al, v.y);
+                  v.z = fmaf(g.z, al, v.z);
+                  v.w = fmaf(g.w, al, v.w);
+                }
+                dst[k] = v;
+              }
+            }
+          }
+        }
+        m_b = mt;
+        l_b = 0.f;
+      } else {
+        const bool need = (mt - m_b) * c2 > kLazyRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? ex2((m_b - mt) * c2) : 1.f;
+          if (need) {
+            l_b *= alpha;
+            m_b = mt;
+          }
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {
+            uint32_t o[16];
+            tmem_ld16(tO + c * 16, o);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            tmem_st16(tO + c * 16, o);
+          }
+        }
+      }
+
+      const float mb2 = m_b * c2;
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const float p = ex2(fmaf(s[c], c2, -mb2));
+        s[c] = p;
+        sum += p;
+      }
+      l_b += sum;
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) pk[k] = pack2<kKvi8r>(s[hlf * 64 + 2 * k], s[hlf * 64 + 2 * k + 1]);
+        tmem_st32(tS + hlf * 32, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.p_full[q]));
+    }
+
+    if (ok && warp_wait(smem_u32(&sm.o_full), 0, wctx)) {
+      // epilogue, phase 1: each thread finishes its own row (final block
+      // merge, 1/Lambda) and stages it in shared memory, fp32, with 16-byte
+      // granule gi of row i at position gi ^ (i mod 32).  The K/V rings are
+      // free now: every MMA has completed and no copy is outstanding.
+      tc_fence_after();
+      uint8_t *stage = sm.k[0] + q * (kNQ * kTileBytes);
+      const int n_blocks = (n_tiles + blk - 1) / blk;
+      float ga, gb;
+      if (n_blocks == 1) {
+        ga = 0.f;
+        gb = 1.f / l_b;
+      } else {
+        const float Mn = fmaxf(M, m_b);
+        const float al = ex2((M - Mn) * c2);
+        const float be = ex2((m_b - Mn) * c2);
+        const float inv = 1.f / (Lam * al + l_b * be);
+        ga = al * inv;
+        gb = be * inv;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float o[32];
+        tmem_ld32(tO + c * 32, *reinterpret_cast<uint32_t(*)[32]>(o));
+#pragma unroll
+        for (int k = 0; k < 32; ++k) o[k] *= gb;
+        if (n_blocks > 1 && row_ok) {
+          const float4 *src = reinterpret_cast<const float4 *>(orow + c * 32);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float4 g = src[k];
+            o[4 * k + 0] = fmaf(g.x, ga, o[4 * k + 0]);
+            o[4 * k + 1] = fmaf(g.y, ga, o[4 * k + 1]);
+            o[4 * k + 2] = fmaf(g.z, ga, o[4 * k + 2]);
+            o[4 * k + 3] = fmaf(g.w, ga, o[4 * k + 3]);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t gi = c * 8 + k;
+          *reinterpret_cast<float4 *>(stage + i * 512 + ((gi ^ (i & 31)) << 4)) =
+              make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+        }
+      }
+      __syncwarp();
+      // phase 2: each warp takes its 32 rows one at a time across the warp:
+      // un-rotate (kvi8r: O = O' H^T, H symmetric) and store coalesced.
+      const int wq = warp & 3;
+#pragma unroll 4
+      for (int rr = 0; rr < 32; ++rr) {
+        const uint32_t ti = wq * 32 + rr;
+        const float4 v = *reinterpret_cast<const float4 *>(stage + ti * 512 + ((lane ^ (ti & 31)) << 4));
+        float x[4] = {v.x, v.y, v.z, v.w};
+        if constexpr (kKvi8r) {
+          fwht128_warp(x, lane);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) x[t] *= kInvSqrt128;
+        }
+        const int64_t r = row0 + q * kBM + ti;
+        if (r < a.q_end)
+          *reinterpret_cast<float4 *>(a.o + (static_cast<int64_t>(h) * a.q_seq + r) * 128 + 4 * lane) =
+              make_float4(x[0], x[1], x[2], x[3]);
+      }
+    }
+  } else if (warp < 12) {
+    // ======================================================= dequantisers
+    reg_dealloc<kKvi8r ? kRegDequantKvi8r : kRegDequantExact>();
+    if constexpr (kKvi8r) {
+      const int dw = warp - 8;
+      const uint16_t *ksc = a.k_scales + static_cast<int64_t>(h) * a.kv_seq;
+      const uint16_t *vsc = a.v_scales + static_cast<int64_t>(h) * a.kv_seq;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int64_t tok0 = static_cast<int64_t>(j) * kBN;
+        const int valid = static_cast<int>(a.kv_seq - tok0 < kBN ? a.kv_seq - tok0 : kBN);
+        const int ks = j % kNK, vs = j % kNV;
+        if (!warp_wait(smem_u32(&sm.k_load[ks]), (j / kNK) & 1, wctx)) break;
+        dequant_tile(sm.k[ks], ksc + tok0, valid, dw, lane);
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&sm.k_ready[ks]));
+        if (!warp_wait(smem_u32(&sm.v_load[vs]), (j / kNV) & 1, wctx)) break;
+        dequant_tile(sm.v[vs], vsc + tok0, valid, dw, lane);
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&sm.v_ready[vs]));
+      }
+    }
+  } else {
+    reg_dealloc<kKvi8r ? kRegIssueKvi8r : kRegIssueExact>();
+    if (warp == 12 && lane == 0) {
+      // ========================================================== producer
+      int k_issued[kNK] = {0, 0, 0};
+      int v_issued[kNV] = {0, 0};
+      if constexpr (!kKvi8r) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        const uint32_t bar = smem_u32(&sm.q_full);
+        mbar_arrive_expect_tx(bar, kNQ * kTileBytes);
+        for (int q = 0; q < kNQ; ++q)
+          for (int c = 0; c < 2; ++c)
+            tma_load_3d(smem_u32(sm.q[q] + c * kChunkBytes), &tm_q, c * 64, static_cast<int32_t>(row0 + q * kBM),
+                        h, bar);
+      }
+      for (int j = 0; j < n_tiles; ++j) {
+        const int64_t tok0 = static_cast<int64_t>(j) * kBN;
+        const int ks = j % kNK, vs = j % kNV;
+        if (!mbar_wait(smem_u32(&sm.k_free[ks]), ((j / kNK) & 1) ^ 1, wctx)) break;
+        {
+          const uint32_t bar = smem_u32(&sm.k_load[ks]);
+          if constexpr (kKvi8r) {
+            const uint32_t bytes = static_cast<uint32_t>((a.kv_seq - tok0 < kBN ? a.kv_seq - tok0 : kBN) * 128);
+            mbar_arrive_expect_tx(bar, bytes);
+            bulk_g2s(smem_u32(sm.k[ks] + kChunkBytes), a.k_codes + (static_cast<int64_t>(h) * a.kv_seq + tok0) * 128,
+                     bytes, bar);
+          } else {
+            mbar_arrive_expect_tx(bar, kTileBytes);
+            tma_load_3d(smem_u32(sm.k[ks]), &tm_k, 0, static_cast<int32_t>(tok0), h, bar);
+            tma_load_3d(smem_u32(sm.k[ks] + kChunkBytes), &tm_k, 64, static_cast<int32_t>(tok0), h, bar);
+          }
+          ++k_issued[ks];
+        }
+        if (!mbar_wait(smem_u32(&sm.v_free[vs]), ((j / kNV) & 1) ^ 1, wctx)) break;
+        {
+          const uint32_t bar = smem_u32(&sm.v_load[vs]);
+          if constexpr (kKvi8r) {
+            const uint32_t bytes = static_cast<uint32_t>((a.kv_seq - tok0 < kBN ? a.kv_seq - tok0 : kBN) * 128);
+            mbar_arrive_expect_tx(bar, bytes);
+            bulk_g2s(smem_u32(sm.v[vs] + kChunkBytes), a.v_codes + (static_cast<int64_t>(h) * a.kv_seq + tok0) * 128,
+                     bytes, bar);
+          } else {
+            mbar_arrive_expect_tx(bar, kTileBytes);
+            tma_load_3d(smem_u32(sm.v[vs]), &tm_v, 0, static_cast<int32_t>(tok0), h, bar);
+            tma_load_3d(smem_u32(sm.v[vs] + kChunkBytes), &tm_v, 64, static_cast<int32_t>(tok0), h, bar);
+          }
+          ++v_issued[vs];
+        }
+      }
+      if (sm.abort) {
+        // every copy this thread issued must land before the CTA exits
+        for (int s = 0; s < kNK; ++s)
+          if (k_issued[s]) mbar_wait_drain(smem_u32(&sm.k_load[s]), (k_issued[s] - 1) & 1, a.timeout_ns);
+        for (int s = 0; s < kNV; ++s)
+          if (v_issued[s]) mbar_wait_drain(smem_u32(&sm.v_load[s]), (v_issued[s] - 1) & 1, a.timeout_ns);
+        if constexpr (!kKvi8r) mbar_wait_drain(smem_u32(&sm.q_full), 0, a.timeout_ns);
+      }
+    } else if (warp == 13 && lane == 0) {
+      // ====================================================== MMA issuer
+      constexpr uint32_t idesc_qk = idesc_f16(!kKvi8r, false, kBM, kBN);
+      constexpr uint32_t idesc_pv = idesc_f16(!kKvi8r, true, kBM, 128);
+      uint64_t *k_rdy = kKvi8r ? sm.k_ready : sm.k_load;
+      uint64_t *v_rdy = kKvi8r ? sm.v_ready : sm.v_load;
+      // Descriptor start addresses advance by adding (byte offset >> 4) to
+      // the low field; every tile lies below 256 KB so the field never wraps.
+      const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[0]), kChunkBytes, 1024);
+      auto issue_qk = [&](int q, int ks) {
+        const uint64_t dq = dq0 + static_cast<uint64_t>(q * (kTileBytes >> 4));
+        const uint64_t dk = dk0 + static_cast<uint64_t>(ks * (kTileBytes >> 4));
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + q * 128, dq + off, dk + off, idesc_qk, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int q, int vs, bool acc) {
+        const uint64_t dv = dv0 + static_cast<uint64_t>(vs * (kTileBytes >> 4));
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + 256 + q * 128, tmem + q * 128 + kk * 8, dv + (kk * 2048 >> 4), idesc_pv,
+                 (acc || kk > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(smem_u32(&sm.q_full), 0, wctx) && mbar_wait(smem_u32(&k_rdy[0]), 0, wctx);
+      if (ok) {
+        tc_fence_after();
+        issue_qk(0, 0);
+        mma_commit(smem_u32(&sm.s_full[0]));
+        issue_qk(1, 0);
+        mma_commit(smem_u32(&sm.s_full[1]));
+        mma_commit(smem_u32(&sm.k_free[0]));
+        for (int j = 0; j < n_tiles && ok; ++j) {
+          const int vs = j % kNV;
+          const bool acc = (j % blk) != 0;
+          const bool more = j + 1 < n_tiles;
+          const int ks1 = (j + 1) % kNK;
+          ok = mbar_wait(smem_u32(&v_rdy[vs]), (j / kNV) & 1, wctx) &&
+               mbar_wait(smem_u32(&sm.p_full[0]), j & 1, wctx);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(0, vs, acc);
+          if (more) {
+            if (!(ok = mbar_wait(smem_u32(&k_rdy[ks1]), ((j + 1) / kNK) & 1, wctx))) break;
+            tc_fence_after();
+            issue_qk(0, ks1);
+            mma_commit(smem_u32(&sm.s_full[0]));
+          }
+          if (!(ok = mbar_wait(smem_u32(&sm.p_full[1]), j & 1, wctx))) break;
+          tc_fence_after();
+          issue_pv(1, vs, acc);
+          mma_commit(smem_u32(&sm.v_free[vs]));
+          if (more) {
+            issue_qk(1, ks1);
+            mma_commit(smem_u32(&sm.s_full[1]));
+            mma_commit(smem_u32(&sm.k_free[ks1]));
+          }
+        }
+        if (ok) mma_commit(smem_u32(&sm.o_full));
+      }
+      // every MMA issued must finish before TMEM is released
+      mma_commit(smem_u32(&sm.drain));
+      mbar_wait_drain(smem_u32(&sm.drain), 0, a.timeout_ns);
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 13) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace attn
+}  // namespace h3kv

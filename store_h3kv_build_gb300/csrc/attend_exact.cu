@@ -1,0 +1,19 @@
+// attend_exact.cu -- exact-store attention launcher (bf16 K/V).
+#include "attend.cuh"
+
+namespace h3kv {
+
+cudaError_t launch_attend_exact(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                                const AttnArgs &args, cudaStream_t stream) {
+  const int64_t rows = args.q_end - args.q_begin;
+  if (rows <= 0 || args.heads <= 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(attn::attend_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(attn::kSmemBytes));
+  if (e != cudaSuccess) return e;
+  const dim3 grid(static_cast<unsigned>((rows + kAttnRowsPerCta - 1) / kAttnRowsPerCta),
+                  static_cast<unsigned>(args.heads));
+  attn::attend_kernel<false><<<grid, attn::kThreads, attn::kSmemBytes, stream>>>(q, k, v, args);
+  return cudaGetLastError();
+}
+
+}  // namespace h3kv

@@ -1,0 +1,50 @@
+// kernels.h -- internal launchers behind the C ABI (not part of the public
+// header).  Every launcher validates nothing: the C-ABI layer has checked the
+// arguments before calling.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace h3kv {
+
+// Store build over `rows` = heads * seq rows of K and V.  Tensor maps: bf16
+// [rows, 128] inputs (box 64 x 128, 128B swizzle) and int8 [rows, 128] code
+// outputs (box 128 x 128, 128B swizzle).
+cudaError_t launch_store_build(const CUtensorMap &k_in, const CUtensorMap &v_in, const CUtensorMap &k_out,
+                               const CUtensorMap &v_out, uint16_t *k_scales, uint16_t *v_scales, int64_t rows,
+                               int num_sms, uint32_t *err, uint64_t timeout_ns, cudaStream_t stream);
+size_t store_build_smem_bytes();
+
+struct AttnArgs {
+  const uint16_t *q;        // bf16 [heads, q_seq, 128]
+  const int8_t *k_codes;    // kvi8r store (unused by the exact path)
+  const int8_t *v_codes;
+  const uint16_t *k_scales;
+  const uint16_t *v_scales;
+  float *o;                 // fp32 [heads, q_seq, 128]
+  int64_t q_seq;
+  int64_t kv_seq;
+  int64_t q_begin;          // this launch's query chunk [q_begin, q_end)
+  int64_t q_end;
+  int32_t heads;
+  int32_t kv_block_tiles;   // 128-key tiles per kv_block
+  float scale_log2;         // softmax_scale * log2(e)
+  uint32_t *err;
+  uint64_t timeout_ns;
+};
+
+constexpr int kAttnRowsPerCta = 256;  // two 128-row query tiles per CTA
+
+// One launch over the query chunk [args.q_begin, args.q_end) of every head.
+// The exact path reads Q, K, V through 3-D tensor maps ({128, seq, heads},
+// box 64 x 128 x 1, 128B swizzle); the kvi8r path reads Q with plain loads
+// and the store with bulk copies (the maps are unused).
+cudaError_t launch_attend_kvi8r(const AttnArgs &args, cudaStream_t stream);
+cudaError_t launch_attend_exact(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                                const AttnArgs &args, cudaStream_t stream);
+size_t attend_smem_bytes();
+
+}  // namespace h3kv

@@ -1,0 +1,205 @@
+// store_build.cu -- the kvi8r store build (kv_store row of the H3 Streamed
+// Blocks Inputs table; kvi8r row of "The K/V store options" table in the Low
+// VRAM write-up): every (token, head) row of K and V is rotated by the fixed
+// orthonormal 128-wide Hadamard basis, given one fp16 absmax scale and
+// quantised to int8.
+//
+// GB300 design: HBM-bound stream.  Rows are flattened over heads (each row is
+// independent).  A persistent grid of CTAs walks 128-row tiles; one producer
+// warp streams bf16 tiles into a 2-stage shared-memory ring with TMA (128-byte
+// swizzle; two CTAs share an SM), four compute warps own one row per thread (the swizzle makes the
+// per-row shared-memory reads bank-conflict free), run the 128-point FWHT in
+// registers, and write codes (swizzled) and scales to a double-buffered output
+// tile that one thread stores with a TMA tensor store and a bulk copy.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace h3kv {
+namespace {
+
+constexpr int kRows = 128;                  // rows per tile = compute threads
+constexpr int kStages = 2;                  // input ring depth (2 CTAs per SM)
+constexpr int kInTileBytes = kRows * 256;   // bf16 [128 x 128]
+constexpr int kOutCodeBytes = kRows * 128;  // int8 [128 x 128]
+constexpr int kThreads = kRows + 32;        // 4 compute warps + 1 producer warp
+
+struct BuildSmem {
+  // 1024-byte aligned tiles first
+  uint8_t in[kStages][kInTileBytes];
+  uint8_t out_codes[2][kOutCodeBytes];
+  uint16_t out_scales[2][kRows];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  int abort;
+};
+
+constexpr size_t kBuildSmemBytes = sizeof(BuildSmem) + 1024;
+
+__global__ void __launch_bounds__(kThreads, 2)
+    store_build_kernel(const __grid_constant__ CUtensorMap tm_k_in, const __grid_constant__ CUtensorMap tm_v_in,
+                       const __grid_constant__ CUtensorMap tm_k_out, const __grid_constant__ CUtensorMap tm_v_out,
+                       uint16_t *__restrict__ k_scales, uint16_t *__restrict__ v_scales, int64_t rows,
+                       int64_t tiles_per_tensor, uint32_t *err, uint64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  BuildSmem &sm = *reinterpret_cast<BuildSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int64_t total_tiles = 2 * tiles_per_tensor;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&sm.full[s]), 1);
+      mbar_init(smem_u32(&sm.empty[s]), kRows);
+    }
+    sm.abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  WaitCtx wctx{err, &sm.abort, timeout_ns};
+
+  if (warp == 4) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_k_in);
+      prefetch_tmap(&tm_v_in);
+      int it = 0;
+      int issued = 0;
+      for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1;
+        if (!mbar_wait(smem_u32(&sm.empty[s]), ph ^ 1, wctx)) break;
+        const bool is_v = t >= tiles_per_tensor;
+        const int32_t row0 = static_cast<int32_t>((is_v ? t - tiles_per_tensor : t) * kRows);
+        const CUtensorMap *map = is_v ? &tm_v_in : &tm_k_in;
+        const uint32_t bar = smem_u32(&sm.full[s]);
+        mbar_arrive_expect_tx(bar, kInTileBytes);
+        tma_load_2d(smem_u32(&sm.in[s][0]), map, 0, row0, bar);
+        tma_load_2d(smem_u32(&sm.in[s][kInTileBytes / 2]), map, 64, row0, bar);
+        ++issued;
+      }
+      if (sm.abort) {
+        // drain: every issued load must land before the CTA may exit
+        for (int k = (issued > kStages ? issued - kStages : 0); k < issued; ++k)
+          mbar_wait_drain(smem_u32(&sm.full[k % kStages]), (k / kStages) & 1, timeout_ns);
+      }
+    }
+  } else {
+    // ----------------------------------------------------------- compute
+    const uint32_t r = static_cast<uint32_t>(tid);  // row within tile
+    int it = 0;
+    for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+      const int s = it % kStages;
+      const uint32_t ph = (it / kStages) & 1;
+      const int b = it & 1;
+      // output tile b must no longer be read by the store of tile it-2
+      if (tid == 0) bulk_wait_read<1>();
+      // every compute thread takes the same decision (a wait that gave up on
+      // one thread stops all of them together)
+      const bool ok = mbar_wait(smem_u32(&sm.full[s]), ph, wctx);
+      if (!named_bar_and(1, kRows, ok)) break;
+
+      // read my row: element e at chunk e/64, granule (e%64)/8, swizzled
+      float x[128];
+      const uint8_t *tile = sm.in[s];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(tile + c * (kInTileBytes / 2) + sw128_off(r, g));
+          const int e = c * 64 + g * 8;
+          x[e + 0] = bf16lo_to_f32(v.x);
+          x[e + 1] = bf16hi_to_f32(v.x);
+          x[e + 2] = bf16lo_to_f32(v.y);
+          x[e + 3] = bf16hi_to_f32(v.y);
+          x[e + 4] = bf16lo_to_f32(v.z);
+          x[e + 5] = bf16hi_to_f32(v.z);
+          x[e + 6] = bf16lo_to_f32(v.w);
+          x[e + 7] = bf16hi_to_f32(v.w);
+        }
+      }
+      mbar_arrive(smem_u32(&sm.empty[s]));
+
+      fwht128(x);  // x now holds sqrt(128) * (row H)
+
+      float amax = 0.f;
+#pragma unroll
+      for (int e = 0; e < 128; ++e) amax = fmaxf(amax, fabsf(x[e]));
+      // s = fp16(absmax(x H) / 127), saturated at the largest finite fp16
+      const float a = amax * kInvSqrt128;
+      __half sh = __float2half_rn(__fdiv_rn(a, 127.0f));
+      bool clamp = false;
+      if (__hisinf(sh)) {
+        sh = __ushort_as_half(0x7BFFu);  // 65504
+        clamp = true;
+      }
+      const float sf = __half2float(sh);
+      clamp = clamp || (sf < 6.103515625e-05f);  // fp16 subnormal scale: x'/s may exceed 127.5
+      const float m = sf > 0.f ? __frcp_rn(sf * 11.313708498984761f) : 0.f;
+
+      // code = rne(x' / s) = rne(x * m) with m = 1 / (sqrt(128) s): adding
+      // 1.5 * 2^23 rounds to an integer held in the low mantissa bits, whose
+      // low byte is the two's-complement int8 code.
+      constexpr float kMagic = 12582912.0f;
+      uint8_t *oc = sm.out_codes[b];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint32_t q[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float v = x[g * 16 + k * 4 + u];
+            q[u] = clamp ? __float_as_uint(fminf(fmaxf(v * m, -127.f), 127.f) + kMagic)
+                         : __float_as_uint(fmaf(v, m, kMagic));
+          }
+          const uint32_t lo = __byte_perm(q[0], q[1], 0x0040);
+          const uint32_t hi = __byte_perm(q[2], q[3], 0x0040);
+          w[k] = __byte_perm(lo, hi, 0x5410);
+        }
+        *reinterpret_cast<uint4 *>(oc + sw128_off(r, g)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      sm.out_scales[b][r] = __half_as_ushort(sh);
+
+      const bool is_v = t >= tiles_per_tensor;
+      const int64_t row0 = (is_v ? t - tiles_per_tensor : t) * kRows;
+      const bool full_tile = row0 + kRows <= rows;
+      uint16_t *scales = is_v ? v_scales : k_scales;
+      if (!full_tile && row0 + r < rows) scales[row0 + r] = __half_as_ushort(sh);
+
+      fence_proxy_async_smem();
+      named_bar_sync(1, kRows);
+      if (tid == 0) {
+        tma_store_2d(is_v ? &tm_v_out : &tm_k_out, 0, static_cast<int32_t>(row0), smem_u32(oc));
+        if (full_tile) bulk_s2g(scales + row0, smem_u32(&sm.out_scales[b][0]), kRows * 2);
+        bulk_commit();
+      }
+    }
+    if (tid == 0) bulk_wait<0>();
+  }
+  __syncthreads();
+}
+
+}  // namespace
+
+size_t store_build_smem_bytes() { return kBuildSmemBytes; }
+
+cudaError_t launch_store_build(const CUtensorMap &k_in, const CUtensorMap &v_in, const CUtensorMap &k_out,
+                               const CUtensorMap &v_out, uint16_t *k_scales, uint16_t *v_scales, int64_t rows,
+                               int num_sms, uint32_t *err, uint64_t timeout_ns, cudaStream_t stream) {
+  static_assert(offsetof(BuildSmem, out_codes) % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
+  const int64_t tiles = (rows + kRows - 1) / kRows;
+  if (tiles == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(store_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kBuildSmemBytes));
+  if (e != cudaSuccess) return e;
+  int64_t grid = static_cast<int64_t>(num_sms) * 2;
+  if (grid > 2 * tiles) grid = 2 * tiles;
+  store_build_kernel<<<static_cast<unsigned>(grid), kThreads, kBuildSmemBytes, stream>>>(
+      k_in, v_in, k_out, v_out, k_scales, v_scales, rows, tiles, err, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace h3kv

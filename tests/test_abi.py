@@ -1,0 +1,89 @@
+"""CPU-side checks of the C-ABI library: it loads, exports every entry point
+that include/h3kv.h declares, and rejects bad arguments on the host before any
+launch (no GPU is needed for any of these)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "h3kv.h")
+
+from store_h3kv_build_gb300 import binding as b  # noqa: E402  (built by conftest if missing)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(h3kv_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert len(names) >= 7
+    lib = ctypes.CDLL(b.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(b.EXPORTED)
+
+
+def test_abi_version_and_strings():
+    assert b.h3kv_abi_version() == 1
+    for st in range(5):
+        assert b.h3kv_strerror(st)
+    assert b.h3kv_strerror(99) == b"unknown status"
+
+
+def test_store_bytes():
+    assert b.h3kv_store_bytes(32, 217088, 128) == 2 * 32 * 217088 * 130
+    assert b.h3kv_store_bytes(1, 0, 128) == 0
+    assert b.h3kv_store_bytes(1, 10, 64) == 0
+    assert b.h3kv_store_bytes(-1, 10, 128) == 0
+
+
+def _store(heads=1, seq=256, ptr=4096, head_dim=128):
+    return b.h3kv_store(ptr, ptr, ptr, ptr, heads, seq, head_dim)
+
+
+def test_build_store_rejects_bad_arguments():
+    st = _store()
+    bs = b.h3kv_build_store
+    assert bs(4096, 4096, 1, 256, 128, None, None) == b.H3KV_ERR_INVALID_ARG          # no store
+    assert bs(4096, 4096, 1, 256, 64, ctypes.byref(st), None) == b.H3KV_ERR_UNSUPPORTED  # head_dim
+    assert bs(4096, 4096, 2, 256, 128, ctypes.byref(st), None) == b.H3KV_ERR_INVALID_ARG  # shape mismatch
+    assert bs(0, 4096, 1, 256, 128, ctypes.byref(st), None) == b.H3KV_ERR_INVALID_ARG     # null K
+    assert bs(4097, 4096, 1, 256, 128, ctypes.byref(st), None) == b.H3KV_ERR_INVALID_ARG  # misaligned
+    assert bs(4096, 4096, -1, 256, 128, ctypes.byref(_store(heads=-1)), None) == b.H3KV_ERR_INVALID_ARG
+    assert bs(0, 0, 0, 0, 128, ctypes.byref(_store(heads=0, seq=0, ptr=0)), None) == b.H3KV_OK  # empty
+
+
+def test_attend_rejects_bad_arguments():
+    st = _store()
+    at = b.h3kv_attend
+    assert at(4096, 256, None, 256, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    assert at(4096, 256, ctypes.byref(st), 0, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG     # q_chunk 0
+    assert at(4096, 256, ctypes.byref(st), 64, 100, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG  # kv_block % 128
+    assert at(4096, 256, ctypes.byref(st), 64, -128, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    assert at(4096, 256, ctypes.byref(_store(head_dim=64)), 64, 0, 0.0, 4096, None) == b.H3KV_ERR_UNSUPPORTED
+    assert at(4104, 256, ctypes.byref(st), 64, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG    # misaligned Q
+    assert at(4096, 256, ctypes.byref(st), 64, 0, 0.0, 0, None) == b.H3KV_ERR_INVALID_ARG       # null O
+    assert at(4096, 256, ctypes.byref(_store(seq=0)), 64, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    assert at(4096, 0, ctypes.byref(st), 64, 0, 0.0, 4096, None) == b.H3KV_OK                  # empty queries
+
+
+def test_attend_exact_rejects_bad_arguments():
+    ae = b.h3kv_attend_exact
+    assert ae(4096, 256, 4096, 4096, 1, 256, 96, 64, 0, 0.0, 4096, None) == b.H3KV_ERR_UNSUPPORTED
+    assert ae(4096, 256, 4096, 4096, 1, 256, 128, 0, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    assert ae(4096, 256, 4096, 4096, 1, 256, 128, 64, 64, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    assert ae(4096, 256, 0, 4096, 1, 256, 128, 64, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    assert ae(4096, 256, 4096, 4096, 1, 0, 128, 64, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    assert ae(4096, 256, 4096, 4104, 1, 256, 128, 64, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    assert ae(4096, 256, 4096, 4096, 0, 256, 128, 64, 0, 0.0, 4096, None) == b.H3KV_OK
+
+
+def test_binding_raises_on_error_status():
+    with pytest.raises(b.H3kvError) as e:
+        b.check(b.H3KV_ERR_INVALID_ARG, "x")
+    assert e.value.status == b.H3KV_ERR_INVALID_ARG
