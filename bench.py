@@ -1,0 +1,366 @@
+"""Benchmark of the kvi8r hot path: build the rotated-int8 store from bf16 K, V
+and attend the whole query sequence over it, on synthetic inputs with the
+shapes of the pages' long-sequence workload (217,088 packed tokens, 32 heads,
+head dim 128, K with 4 outlier channels x20).
+
+One step = h3kv_build_store + h3kv_attend (q_chunk 16384, kv_block 16384) over
+one batch of inputs already resident in HBM.  Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+`--impl reference` times the fp64 CPU oracle (the only reference this method
+has) on the host cores, on bounded samples of the same workload.  Under
+torchrun (N > 1) every rank runs its own replica of the workload on its GPU
+(the path shards by heads with no exchange, so this is weak scaling with no
+collective on the data path); timings are the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from store_h3kv_build_gb300 import synth  # noqa: E402
+
+METRIC = "kvi8r attention TFLOP/s at 217k tokens (1 GB300) + store-build GB/s"
+UNIT = "TFLOP/s"
+HEAD_DIM = 128
+KERNEL_SOURCES = ["store_h3kv_build_gb300/csrc/attend.cuh", "store_h3kv_build_gb300/csrc/attend_kvi8r.cu",
+                  "store_h3kv_build_gb300/csrc/ptx.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attend_kvi8r_traffic.json")
+
+
+def attention_flops(heads, q_seq, kv_seq):
+    """Algorithmic FLOPs of one attention pass: QK^T and PV, 2 flops per MAC."""
+    return 4.0 * heads * q_seq * kv_seq * HEAD_DIM
+
+
+def store_bytes(heads, seq):
+    """Algorithmic bytes of one store build: read bf16 K and V, write int8
+    codes and fp16 scales for both."""
+    rows = heads * seq
+    return 2 * rows * HEAD_DIM * 2 + 2 * rows * HEAD_DIM + 2 * rows * 2
+
+
+def workload_desc(name, w):
+    return {
+        "workload": f"{name}: {w['heads']} heads x {w['seq']} tokens x d{HEAD_DIM}, bf16 Q/K/V ~N(0,1)"
+                    + (", K outlier channels x20" if w["k_outliers"] else "")
+                    + f", non-causal, q_chunk {w['q_chunk']}, kv_block {w['kv_block']}",
+        "heads": w["heads"], "seq": w["seq"], "head_dim": HEAD_DIM,
+        "q_chunk": w["q_chunk"], "kv_block": w["kv_block"],
+        "l2": "no flush: every step streams inputs far larger than the 129 MB L2",
+    }
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_sha():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(launches_per_call):
+    """DRAM bytes per attention launch from the committed ncu summary, if that
+    summary was taken on the current kernel source (else None)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    d = json.load(open(TRAFFIC_FILE))
+    if d.get("kernel_src_sha") != kernel_sha():
+        return None
+    return d.get("dram_bytes_per_full_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.lines = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def time_oracle_sample(w, rows=512, head=0, seed=0):
+    """The fp64 oracle on a bounded sample of the workload: build the store of
+    one head (all `seq` tokens of K and V) and attend `rows` query rows of that
+    head over it.  Returns (attention TFLOP/s, store GB/s, seconds, desc)."""
+    import oracle
+    q = synth.normal_bf16((1, rows, HEAD_DIM), seed + 100)
+    k = synth.make_k(1, w["seq"], seed + 101, w["k_outliers"])
+    v = synth.normal_bf16((1, w["seq"], HEAD_DIM), seed + 102)
+    t0 = time.perf_counter()
+    st = oracle.build_store(k, v)
+    t1 = time.perf_counter()
+    oracle.attend(q, st)
+    t2 = time.perf_counter()
+    att = attention_flops(1, rows, w["seq"]) / (t2 - t1) / 1e12
+    gbs = store_bytes(1, w["seq"]) / (t1 - t0) / 1e9
+    desc = (f"oracle (NumPy fp64): store of 1 head x {w['seq']} tokens, then {rows} query rows of that head "
+            f"attended over all {w['seq']} keys")
+    return att, gbs, t2 - t0, desc
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        return max((i.get("num_threads", 1) for i in info), default=os.cpu_count())
+    except Exception:
+        return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+def run_reference(args, w, name):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return 0
+    for _ in range(args.warmup):
+        time_oracle_sample(w, rows=args.ref_rows)
+    vals, gbs_all, secs = [], [], []
+    for _ in range(args.steps):
+        att, gbs, s, desc = time_oracle_sample(w, rows=args.ref_rows)
+        vals.append(att)
+        gbs_all.append(gbs)
+        secs.append(s)
+    value = statistics.median(vals)
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_desc(name, w),
+        "store_build": {"value": statistics.median(gbs_all), "unit": "GB/s"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w, name):
+    from store_h3kv_build_gb300 import binding as b
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = world > 1
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if dist:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=dev)
+
+    H, L = w["heads"], w["seq"]
+    q_chunk, kv_block = w["q_chunk"], w["kv_block"]
+    q, k, v = synth.make_qkv(H, L, seed=0, k_outliers=w["k_outliers"], device=dev)
+    st = b.Store.empty(H, L, dev)
+    out = torch.empty((H, L, HEAD_DIM), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    n_chunks = (L + q_chunk - 1) // q_chunk
+    launches_per_step = 1 + n_chunks
+
+    def step():
+        b.build_store(k, v, out=st)
+        b.attend(q, st, q_chunk=q_chunk, kv_block=kv_block, out=out)
+
+    def barrier():
+        if dist:
+            import torch.distributed as tdist
+            tdist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    b.sync_status()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else local
+    barrier()
+    with ClockSampler(gpu_index) as clocks:
+        t_wall = time.perf_counter()
+        for e0, e1, e2 in ev:
+            e0.record(stream)
+            b.build_store(k, v, out=st)
+            e1.record(stream)
+            b.attend(q, st, q_chunk=q_chunk, kv_block=kv_block, out=out)
+            e2.record(stream)
+        barrier()
+        t_wall = time.perf_counter() - t_wall
+    b.sync_status()
+    build_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev]
+    attend_ms = [e1.elapsed_time(e2) for _, e1, e2 in ev]
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    t = torch.tensor([total_ms, sum(build_ms), sum(attend_ms)], dtype=torch.float64, device=dev)
+    if dist:
+        import torch.distributed as tdist
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    total_ms, build_sum, attend_sum = t.tolist()
+    ms_per_step = total_ms / args.steps
+    flops = attention_flops(H, L, L)
+    value = world * flops * args.steps / (total_ms / 1e3) / 1e12
+
+    # ---- end to end through the public API with host buffers
+    hq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    hk = torch.empty(k.shape, dtype=k.dtype, pin_memory=True)
+    hv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+    hq.copy_(q)
+    hk.copy_(k)
+    hv.copy_(v)
+    ho = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    e2e_steps = max(1, min(args.steps, 3))
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        b.build_store(k, v, out=st)
+        b.attend(q, st, q_chunk=q_chunk, kv_block=kv_block, out=out)
+        ho.copy_(out, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    es.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ee.record(stream)
+    barrier()
+    e2e_ms = es.elapsed_time(ee)
+    te = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+    if dist:
+        import torch.distributed as tdist
+        tdist.all_reduce(te, op=tdist.ReduceOp.MAX)
+    e2e_ms = te.item()
+    e2e_value = world * flops * e2e_steps / (e2e_ms / 1e3) / 1e12
+    h2d = (q.numel() + k.numel() + v.numel()) * 2
+    d2h = out.numel() * 4
+    b.sync_status()
+
+    if rank == 0:
+        peaks, peak_src = load_peaks()
+        peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+        achieved = flops * args.steps / (attend_sum / 1e3) / 1e12
+        traffic = recorded_traffic(n_chunks)
+        build_gbs = store_bytes(H, L) * args.steps / (build_sum / 1e3) / 1e9
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp16", "data": "synthetic", "config": workload_desc(name, w),
+            "store_build": {"value": build_gbs, "unit": "GB/s", "ms": build_sum / args.steps,
+                            "bytes": store_bytes(H, L), "frac_of_hbm": build_gbs / peaks["hbm_gbs"],
+                            "hbm_peak_gbs": peaks["hbm_gbs"]},
+            "attend_ms": attend_sum / args.steps,
+            "roofline": {"bound": "tensor", "kernel": "attend_kernel<kvi8r>", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_source": f"{peak_src} bf16_tflops_sustained (fp16 dense rate = bf16)",
+                         "frac_of_burst": achieved / peaks["bf16_tflops"],
+                         "traffic": traffic, "launches_per_step": n_chunks,
+                         "flops_per_step": flops},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks.summary(),
+            "wall_s_timed": t_wall,
+        }
+        if not args.no_cpu_baseline:
+            att, gbs, s, desc = time_oracle_sample(w, rows=args.ref_rows)
+            line["cpu_baseline"] = {"value": att, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                                    "sample": desc, "store_gbs": gbs, "seconds": s}
+        print(json.dumps(line), flush=True)
+    if dist:
+        import torch.distributed as tdist
+        tdist.barrier()
+        tdist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="h32_l217088_outlier", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--ref-rows", type=int, default=2048, help="query rows in the oracle's bounded sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="omit the oracle timing (used for profiler runs only)")
+    args = ap.parse_args()
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w, args.workload)
+    return run_ours(args, w, args.workload)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

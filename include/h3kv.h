@@ -117,6 +117,20 @@ h3kv_status h3kv_attend_exact(const uint16_t *Q, int64_t q_seq, const uint16_t *
  * H3KV_ERR_CUDA if the synchronisation itself reports an error. */
 h3kv_status h3kv_sync_status(void *stream);
 
+/* Set the limit (nanoseconds) of every bounded in-kernel wait in later
+ * launches; 0 restores the default of 1 s.  Process-wide.  A limit far below
+ * the kernels' normal waits makes them give up early: the launch then
+ * records H3KV_ERR_DEVICE_TIMEOUT, drains its own copies and MMAs, and exits
+ * with its output undefined, leaving the context usable. */
+h3kv_status h3kv_set_wait_timeout_ns(uint64_t timeout_ns);
+
+/* Diagnostic of the failure path (no counterpart on the pages): launch one
+ * CTA whose only wait is on a barrier that nothing ever arrives on, limited
+ * to `timeout_ns` (0 = default).  The wait runs out, the kernel records
+ * H3KV_ERR_DEVICE_TIMEOUT in the device error word and returns, so the next
+ * h3kv_sync_status() on `stream` reports it.  Nothing faults or traps. */
+h3kv_status h3kv_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
+
 /* Static description of a status code (never NULL). */
 const char *h3kv_strerror(h3kv_status status);
 

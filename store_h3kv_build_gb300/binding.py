@@ -49,6 +49,8 @@ _SIGS = {
     "h3kv_attend": (ctypes.c_int, [_vp, _i64, ctypes.POINTER(h3kv_store), _i32, _i32, _f32, _vp, _vp]),
     "h3kv_attend_exact": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _f32, _vp, _vp]),
     "h3kv_sync_status": (ctypes.c_int, [_vp]),
+    "h3kv_set_wait_timeout_ns": (ctypes.c_int, [ctypes.c_uint64]),
+    "h3kv_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _vp]),
     "h3kv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
 }
 for _name, (_res, _args) in _SIGS.items():

@@ -3,10 +3,12 @@
 // error word.
 #include <cudaTypedefs.h>
 #include <math.h>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/h3kv.h"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace {
 
@@ -17,6 +19,24 @@ __device__ uint32_t g_h3kv_error;
 
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s per bounded wait
+std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
+
+// One CTA waits on an mbarrier that nothing ever arrives on: the bounded wait
+// runs out, records the timeout in the device error word and the kernel
+// returns.  No fault, no trap; the context stays usable.
+__global__ void wait_selftest_kernel(uint32_t *err, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    h3kv::mbar_init(h3kv::smem_u32(&bar), 1);
+    abort_flag = 0;
+    h3kv::fence_mbar_init();
+  }
+  __syncthreads();
+  const h3kv::WaitCtx w{err, &abort_flag, timeout_ns};
+  h3kv::mbar_wait(h3kv::smem_u32(&bar), 0, w);
+  __syncthreads();
+}
 
 struct DeviceInfo {
   bool ready = false;
@@ -147,7 +167,7 @@ h3kv_status h3kv_build_store(const uint16_t *K, const uint16_t *V, int32_t heads
       !encode_2d(&v_out, CU_TENSOR_MAP_DATA_TYPE_UINT8, out->v_codes, rows, 1, 128))
     return H3KV_ERR_CUDA;
   const cudaError_t e = h3kv::launch_store_build(k_in, v_in, k_out, v_out, out->k_scales, out->v_scales, rows,
-                                                 d->num_sms, d->err, kDefaultTimeoutNs,
+                                                 d->num_sms, d->err, g_timeout_ns.load(),
                                                  static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? H3KV_OK : H3KV_ERR_CUDA;
 }
@@ -184,7 +204,7 @@ h3kv_status h3kv_attend(const uint16_t *Q, int64_t q_seq, const h3kv_store *stor
   a.kv_block_tiles = kvb / H3KV_KV_TILE;
   a.scale_log2 = scale_log2_of(softmax_scale);
   a.err = d->err;
-  a.timeout_ns = kDefaultTimeoutNs;
+  a.timeout_ns = g_timeout_ns.load();
   for (int64_t c0 = 0; c0 < q_seq; c0 += q_chunk) {
     a.q_begin = c0;
     a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
@@ -224,7 +244,7 @@ h3kv_status h3kv_attend_exact(const uint16_t *Q, int64_t q_seq, const uint16_t *
   a.kv_block_tiles = kv_block == 0 ? static_cast<int32_t>(n_tiles) : kv_block / H3KV_KV_TILE;
   a.scale_log2 = scale_log2_of(softmax_scale);
   a.err = d->err;
-  a.timeout_ns = kDefaultTimeoutNs;
+  a.timeout_ns = g_timeout_ns.load();
   for (int64_t c0 = 0; c0 < q_seq; c0 += q_chunk) {
     a.q_begin = c0;
     a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
@@ -232,6 +252,20 @@ h3kv_status h3kv_attend_exact(const uint16_t *Q, int64_t q_seq, const uint16_t *
       return H3KV_ERR_CUDA;
   }
   return H3KV_OK;
+}
+
+h3kv_status h3kv_set_wait_timeout_ns(uint64_t timeout_ns) {
+  g_timeout_ns.store(timeout_ns == 0 ? kDefaultTimeoutNs : timeout_ns);
+  return H3KV_OK;
+}
+
+h3kv_status h3kv_selftest_wait_timeout(uint64_t timeout_ns, void *stream) {
+  DeviceInfo *d = nullptr;
+  h3kv_status st = device_info(&d);
+  if (st != H3KV_OK) return st;
+  wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      d->err, timeout_ns == 0 ? kDefaultTimeoutNs : timeout_ns);
+  return cudaGetLastError() == cudaSuccess ? H3KV_OK : H3KV_ERR_CUDA;
 }
 
 h3kv_status h3kv_sync_status(void *stream) {

@@ -455,10 +455,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (sm.abort) {
         // every copy this thread issued must land before the CTA exits
         for (int s = 0; s < kNK; ++s)
-          if (k_issued[s]) mbar_wait_drain(smem_u32(&sm.k_load[s]), (k_issued[s] - 1) & 1, a.timeout_ns);
+          if (k_issued[s]) mbar_wait_drain(smem_u32(&sm.k_load[s]), (k_issued[s] - 1) & 1, kDrainNs);
         for (int s = 0; s < kNV; ++s)
-          if (v_issued[s]) mbar_wait_drain(smem_u32(&sm.v_load[s]), (v_issued[s] - 1) & 1, a.timeout_ns);
-        if constexpr (!kKvi8r) mbar_wait_drain(smem_u32(&sm.q_full), 0, a.timeout_ns);
+          if (v_issued[s]) mbar_wait_drain(smem_u32(&sm.v_load[s]), (v_issued[s] - 1) & 1, kDrainNs);
+        if constexpr (!kKvi8r) mbar_wait_drain(smem_u32(&sm.q_full), 0, kDrainNs);
       }
     } else if (warp == 13 && lane == 0) {
       // ====================================================== MMA issuer
@@ -525,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // every MMA issued must finish before TMEM is released
       mma_commit(smem_u32(&sm.drain));
-      mbar_wait_drain(smem_u32(&sm.drain), 0, a.timeout_ns);
+      mbar_wait_drain(smem_u32(&sm.drain), 0, kDrainNs);
     }
   }
   __syncwarp();

@@ -17,6 +17,10 @@ namespace h3kv {
 // ---------------------------------------------------------------------------
 enum : uint32_t { kErrTimeout = 1u };
 
+// Limit for the waits that drain a CTA's own copies and MMAs after an abort.
+// Those always complete within microseconds; the limit only guards exit.
+constexpr uint64_t kDrainNs = 1000000000ull;
+
 struct WaitCtx {
   uint32_t *err;          // device error word (global)
   volatile int *abort;    // CTA-local abort flag (shared)
@@ -72,10 +76,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity.  Returns false (after
 // recording the timeout) if the limit ran out or another role aborted.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx &w) {
-  if (mbar_try_wait(bar, parity)) return true;
+  // the limit counts from the start of the wait (one timer read up front)
   const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+  while (!mbar_try_wait(bar, parity)) {
     if (*w.abort) return false;
     if (globaltimer_ns() - t0 > w.timeout_ns) {
       atomicOr(w.err, kErrTimeout);
@@ -83,6 +86,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
       return false;
     }
   }
+  return true;
 }
 
 // Bounded wait used while draining after an abort: ignores the abort flag.

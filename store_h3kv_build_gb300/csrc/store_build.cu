@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (sm.abort) {
         // drain: every issued load must land before the CTA may exit
         for (int k = (issued > kStages ? issued - kStages : 0); k < issued; ++k)
-          mbar_wait_drain(smem_u32(&sm.full[k % kStages]), (k / kStages) & 1, timeout_ns);
+          mbar_wait_drain(smem_u32(&sm.full[k % kStages]), (k / kStages) & 1, kDrainNs);
       }
     }
   } else {

@@ -87,3 +87,8 @@ def test_binding_raises_on_error_status():
     with pytest.raises(b.H3kvError) as e:
         b.check(b.H3KV_ERR_INVALID_ARG, "x")
     assert e.value.status == b.H3KV_ERR_INVALID_ARG
+
+
+def test_wait_timeout_setter_needs_no_device():
+    assert b.h3kv_set_wait_timeout_ns(5000) == b.H3KV_OK
+    assert b.h3kv_set_wait_timeout_ns(0) == b.H3KV_OK

@@ -1,0 +1,65 @@
+"""Failure detection on the GPU without faulting it.
+
+Every wait in the kernels is bounded.  These tests make waits run out on
+purpose -- one on a barrier that nothing ever arrives on, and the real
+kernels under a wait limit far below their normal waits -- and check that the
+host reads H3KV_ERR_DEVICE_TIMEOUT, that the error word clears, and that the
+context still computes correct results afterwards.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import compare_attention
+from store_h3kv_build_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _b():
+    from store_h3kv_build_gb300 import binding as b
+    return b
+
+
+def _tiny_check(cuda):
+    b = _b()
+    q, k, v = synth.make_qkv(1, 1024, seed=0)
+    st = b.build_store(k.to(cuda), v.to(cuda))
+    out = b.attend(q.to(cuda), st, q_chunk=256, kv_block=512)
+    b.sync_status()
+    compare_attention(out, oracle.attend(q, oracle.build_store(k, v)), "after timeout")
+
+
+def test_selftest_wait_runs_out_and_context_survives(cuda):
+    b = _b()
+    s = torch.cuda.current_stream().cuda_stream
+    assert b.h3kv_sync_status(s) == b.H3KV_OK
+    assert b.h3kv_selftest_wait_timeout(2_000_000, s) == b.H3KV_OK  # 2 ms limit
+    assert b.h3kv_sync_status(s) == b.H3KV_ERR_DEVICE_TIMEOUT
+    assert b.h3kv_sync_status(s) == b.H3KV_OK  # cleared
+    _tiny_check(cuda)
+
+
+@pytest.mark.parametrize("path", ["store", "kvi8r", "exact"])
+def test_kernels_give_up_under_tiny_wait_limit(cuda, path):
+    b = _b()
+    s = torch.cuda.current_stream().cuda_stream
+    q, k, v = synth.make_qkv(2, 4096, seed=3)
+    q, k, v = q.to(cuda), k.to(cuda), v.to(cuda)
+    st = b.build_store(k, v)
+    assert b.h3kv_sync_status(s) == b.H3KV_OK
+    b.check(b.h3kv_set_wait_timeout_ns(1))
+    try:
+        if path == "store":
+            b.build_store(k, v, out=st)
+        elif path == "kvi8r":
+            b.attend(q, st, q_chunk=4096, kv_block=0)
+        else:
+            b.attend_exact(q, k, v, q_chunk=4096, kv_block=0)
+        status = b.h3kv_sync_status(s)
+    finally:
+        b.check(b.h3kv_set_wait_timeout_ns(0))
+    assert status == b.H3KV_ERR_DEVICE_TIMEOUT
+    assert b.h3kv_sync_status(s) == b.H3KV_OK
+    _tiny_check(cuda)
