@@ -48,7 +48,7 @@ constexpr float kLazyRescaleLog2 = 8.0f;    // rescale O only when the max grows
 // 128 (512 threads x 128 = the 64K register file); each split below sums to
 // the same total: 128 x (2 x softmax + dequant + issue) = 65536.
 constexpr uint32_t kRegSoftmax = 184;
-constexpr uint32_t kRegDequantKvi8r = 64, kRegIssueKvi8r = 80;
+constexpr uint32_t kRegDequantKvi8r = 72, kRegIssueKvi8r = 72;
 constexpr uint32_t kRegDequantExact = 56, kRegIssueExact = 88;
 static_assert(2 * kRegSoftmax + kRegDequantKvi8r + kRegIssueKvi8r == 512, "register split");
 static_assert(2 * kRegSoftmax + kRegDequantExact + kRegIssueExact == 512, "register split");
@@ -60,7 +60,7 @@ struct Smem {
   uint64_t q_full;
   uint64_t k_load[kNK], k_ready[kNK], k_free[kNK];
   uint64_t v_load[kNV], v_ready[kNV], v_free[kNV];
-  uint64_t s_full[kNQ], p_full[kNQ];
+  uint64_t s_full[kNQ], p_lo[kNQ], p_hi[kNQ];  // P columns 0-63 / 64-127 ready
   uint64_t o_full;
   uint64_t drain;
   uint32_t tmem_base;
@@ -94,24 +94,43 @@ __device__ __forceinline__ void dequant16(const uint4 raw, const __half2 s2, uin
   }
 }
 
+// Row and 16-byte code granule handled by `lane` in iteration `it` of dequant
+// warp `dw`: each instruction covers 4 rows; a quarter-warp takes 4 granules
+// of an even row and the other-half 4 granules of the next (odd) row, so its
+// 16-byte loads (linear codes) and its 16-byte stores (swizzled fp16) each
+// touch 8 distinct bank groups.
+__device__ __forceinline__ uint32_t dq_row(int dw, int it, int lane) {
+  const int q4 = lane >> 3, hf = (lane >> 2) & 1;
+  return dw * 32 + it * 4 + 2 * (q4 >> 1) + hf;
+}
+__device__ __forceinline__ uint32_t dq_granule(int lane) {
+  const int q4 = lane >> 3, hf = (lane >> 2) & 1;
+  return (lane & 3) + 4 * (hf ^ (q4 & 1));
+}
+
+// Scales of the rows this lane dequantises (rows past `valid` get 0).
+__device__ __forceinline__ void dequant_scales(const uint16_t *scales, int valid, int dw, int lane,
+                                               uint16_t (&sc)[8]) {
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int r = static_cast<int>(dq_row(dw, it, lane));
+    sc[it] = r < valid ? scales[r] : 0;
+  }
+}
+
 // In-place dequantisation of one K or V tile by the 128 dequant threads.
 // On entry the int8 codes of the tile's rows sit linearly (128 bytes per row)
 // in the second half of the tile buffer; on exit the whole buffer holds the
 // fp16 tile in the 128B-swizzled layout the MMA descriptors expect (two
 // 64-column halves of [128 rows x 128 bytes]).  Row r's codes share their
-// 128-byte slot with row r's fp16 columns 64-127, and each row is read by its
-// own 8 lanes in one instruction before they write it, so in place is safe.
-__device__ __forceinline__ void dequant_tile(uint8_t *tile, const uint16_t *scales, int valid, int dw, int lane) {
-  const uint32_t g = lane & 7;
-  uint16_t sc[8];
+// 128-byte slot with row r's fp16 columns 64-127, and every row is read by
+// one load instruction of its warp before any lane writes it, so in place is
+// safe.
+__device__ __forceinline__ void dequant_tile(uint8_t *tile, const uint16_t (&sc)[8], int dw, int lane) {
+  const uint32_t g = dq_granule(lane);
 #pragma unroll
   for (int it = 0; it < 8; ++it) {
-    const int r = dw * 32 + it * 4 + (lane >> 3);
-    sc[it] = r < valid ? scales[r] : 0;
-  }
-#pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    const uint32_t r = dw * 32 + it * 4 + (lane >> 3);
+    const uint32_t r = dq_row(dw, it, lane);
     const uint4 raw = *reinterpret_cast<const uint4 *>(tile + kChunkBytes + r * 128 + g * 16);
     const __half s = __ushort_as_half(sc[it]);
     uint32_t o[8];
@@ -158,7 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int q = 0; q < kNQ; ++q) {
       mbar_init(smem_u32(&sm.s_full[q]), 1);
-      mbar_init(smem_u32(&sm.p_full[q]), kBM);
+      mbar_init(smem_u32(&sm.p_lo[q]), kBM);
+      mbar_init(smem_u32(&sm.p_hi[q]), kBM);
     }
     mbar_init(smem_u32(&sm.o_full), 1);
     mbar_init(smem_u32(&sm.drain), 1);
@@ -226,16 +246,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       float s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+      tmem_ld128(tS, *reinterpret_cast<uint32_t(*)[128]>(s));
       const int64_t valid = a.kv_seq - static_cast<int64_t>(j) * kBN;
       if (valid < kBN) {
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = (c < valid) ? s[c] : -INFINITY;
       }
-      float mt = s[0];
+      float mt;
+      {
+        float m4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mt = fmaxf(mt, s[c]);
+        for (int c = 4; c < 128; c += 8) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) m4[u] = fmax3(m4[u], s[c + 2 * u], s[c + 2 * u + 1]);
+        }
+        mt = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+      }
 
       if (j % blk == 0) {
         if (j > 0) {
@@ -295,25 +321,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 
-      const float mb2 = m_b * c2;
-      float sum = 0.f;
-#pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float p = ex2(fmaf(s[c], c2, -mb2));
-        s[c] = p;
-        sum += p;
-      }
-      l_b += sum;
+      // p = 2^(s c - m c) in packed pairs; P leaves in two halves so the
+      // first half of P.V can start while the second half is computed.
+      const float2 cc = make_float2(c2, c2);
+      const float2 nm = make_float2(-m_b * c2, -m_b * c2);
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int hlf = 0; hlf < 2; ++hlf) {
         uint32_t pk[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) pk[k] = pack2<kKvi8r>(s[hlf * 64 + 2 * k], s[hlf * 64 + 2 * k + 1]);
+        for (int k = 0; k < 32; ++k) {
+          const int c = hlf * 64 + 2 * k;
+          float2 t = __ffma2_rn(make_float2(s[c], s[c + 1]), cc, nm);
+          t.x = ex2(t.x);
+          t.y = ex2(t.y);
+          if (k & 1) acc1 = __fadd2_rn(acc1, t);
+          else acc0 = __fadd2_rn(acc0, t);
+          pk[k] = pack2<kKvi8r>(t.x, t.y);
+        }
         tmem_st32(tS + hlf * 32, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(hlf == 0 ? &sm.p_lo[q] : &sm.p_hi[q]));
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.p_full[q]));
+      const float2 acc = __fadd2_rn(acc0, acc1);
+      l_b += acc.x + acc.y;
     }
 
     if (ok && warp_wait(smem_u32(&sm.o_full), 0, wctx)) {
@@ -387,16 +419,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int dw = warp - 8;
       const uint16_t *ksc = a.k_scales + static_cast<int64_t>(h) * a.kv_seq;
       const uint16_t *vsc = a.v_scales + static_cast<int64_t>(h) * a.kv_seq;
+      uint16_t sck[8], scv[8];
       for (int j = 0; j < n_tiles; ++j) {
         const int64_t tok0 = static_cast<int64_t>(j) * kBN;
         const int valid = static_cast<int>(a.kv_seq - tok0 < kBN ? a.kv_seq - tok0 : kBN);
         const int ks = j % kNK, vs = j % kNV;
+        // scale loads go out before the waits so their latency hides there
+        dequant_scales(ksc + tok0, valid, dw, lane, sck);
+        dequant_scales(vsc + tok0, valid, dw, lane, scv);
         if (!warp_wait(smem_u32(&sm.k_load[ks]), (j / kNK) & 1, wctx)) break;
-        dequant_tile(sm.k[ks], ksc + tok0, valid, dw, lane);
+        dequant_tile(sm.k[ks], sck, dw, lane);
         fence_proxy_async_smem();
         mbar_arrive(smem_u32(&sm.k_ready[ks]));
         if (!warp_wait(smem_u32(&sm.v_load[vs]), (j / kNV) & 1, wctx)) break;
-        dequant_tile(sm.v[vs], vsc + tok0, valid, dw, lane);
+        dequant_tile(sm.v[vs], scv, dw, lane);
         fence_proxy_async_smem();
         mbar_arrive(smem_u32(&sm.v_ready[vs]));
       }
@@ -480,10 +516,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(tmem + q * 128, dq + off, dk + off, idesc_qk, kk > 0);
         }
       };
-      auto issue_pv = [&](int q, int vs, bool acc) {
+      // P.V in two halves of the key tile (P columns 0-63, 64-127)
+      auto issue_pv = [&](int q, int vs, bool acc, int hlf) {
         const uint64_t dv = dv0 + static_cast<uint64_t>(vs * (kTileBytes >> 4));
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
+        for (int kk = hlf * 4; kk < hlf * 4 + 4; ++kk)
           mma_ts(tmem + 256 + q * 128, tmem + q * 128 + kk * 8, dv + (kk * 2048 >> 4), idesc_pv,
                  (acc || kk > 0) ? 1u : 0u);
       };
@@ -501,19 +538,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool more = j + 1 < n_tiles;
           const int ks1 = (j + 1) % kNK;
           ok = mbar_wait(smem_u32(&v_rdy[vs]), (j / kNV) & 1, wctx) &&
-               mbar_wait(smem_u32(&sm.p_full[0]), j & 1, wctx);
+               mbar_wait(smem_u32(&sm.p_lo[0]), j & 1, wctx);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(0, vs, acc);
+          issue_pv(0, vs, acc, 0);
+          if (!(ok = mbar_wait(smem_u32(&sm.p_hi[0]), j & 1, wctx))) break;
+          tc_fence_after();
+          issue_pv(0, vs, acc, 1);
           if (more) {
             if (!(ok = mbar_wait(smem_u32(&k_rdy[ks1]), ((j + 1) / kNK) & 1, wctx))) break;
             tc_fence_after();
             issue_qk(0, ks1);
             mma_commit(smem_u32(&sm.s_full[0]));
           }
-          if (!(ok = mbar_wait(smem_u32(&sm.p_full[1]), j & 1, wctx))) break;
+          if (!(ok = mbar_wait(smem_u32(&sm.p_lo[1]), j & 1, wctx))) break;
           tc_fence_after();
-          issue_pv(1, vs, acc);
+          issue_pv(1, vs, acc, 0);
+          if (!(ok = mbar_wait(smem_u32(&sm.p_hi[1]), j & 1, wctx))) break;
+          tc_fence_after();
+          issue_pv(1, vs, acc, 1);
           mma_commit(smem_u32(&sm.v_free[vs]));
           if (more) {
             issue_qk(1, ks1);
