@@ -13,9 +13,8 @@
 //
 // One CTA owns 256 query rows of one head (two 128-row tiles, so that the
 // softmax of one tile overlaps the tensor-core work of the other) and walks
-// every key of that head in a fixed order -- K/V staged in 128-key tiles,
-// scores in 64-key sub-tiles -- so a query row's arithmetic never depends on
-// q_chunk or on which CTA holds it.
+// every 128-key tile of that head in a fixed order, so a query row's
+// arithmetic never depends on q_chunk or on which CTA holds it.
 //
 // Warp roles (512 threads):
 //   warps 0-3   softmax / correction / epilogue of query tile 0 (thread = row)
@@ -24,11 +23,9 @@
 //   warp 12     producer: TMA / bulk copies of Q (exact) and K/V tiles
 //   warp 13     TMEM allocation and tcgen05.mma issue (one thread)
 //   warps 14-15 idle
-// TMEM (512 columns x 128 lanes, fp32): query tile q has two 64-column score
-// buffers at [128q, 128q+64) and [128q+64, 128q+128) (S double-buffered, so
-// QK^T of sub-tile t+1 runs while the softmax of sub-tile t does), with P
-// (fp16/bf16 pairs) written over the first 32 columns of its buffer, and
-// its output accumulator O_q at [256+128q, 384+128q).
+// TMEM (512 columns x 128 lanes, fp32): S0 [0,128), S1 [128,256) with P0/P1
+// (fp16/bf16 pairs) written over the first 64 columns of S0/S1, O0
+// [256,384), O1 [384,512).
 #pragma once
 
 #include "kernels.h"
@@ -39,20 +36,20 @@ namespace attn {
 
 constexpr int kBM = 128;                    // query rows per tile (MMA M)
 constexpr int kNQ = 2;                      // query tiles per CTA
-constexpr int kBN = 128;                    // keys per staged K/V tile
-constexpr int kSub = 64;                    // keys per score sub-tile (S double-buffered)
+constexpr int kBN = 128;                    // keys per tile
 constexpr int kNK = 3;                      // K tile ring depth
 constexpr int kNV = 2;                      // V tile ring depth
 constexpr int kTileBytes = 128 * 128 * 2;   // one 16-bit [128 x 128] tile
 constexpr int kChunkBytes = kTileBytes / 2; // 64-column half (one swizzle atom wide)
 constexpr int kThreads = 512;
+constexpr int kWarpsPerGroup = 4;           // arrivals on a barrier released by a warpgroup
 constexpr float kLazyRescaleLog2 = 8.0f;    // rescale O only when the max grows by > 2^8
 
 // Register split per warpgroup (setmaxnreg).  The launch gives every thread
 // 128 (512 threads x 128 = the 64K register file); each split below sums to
 // the same total: 128 x (2 x softmax + dequant + issue) = 65536.
-constexpr uint32_t kRegSoftmaxKvi8r = 160, kRegDequantKvi8r = 96, kRegIssueKvi8r = 96;
-constexpr uint32_t kRegSoftmaxExact = 168, kRegDequantExact = 56, kRegIssueExact = 120;
+constexpr uint32_t kRegSoftmaxKvi8r = 184, kRegDequantKvi8r = 72, kRegIssueKvi8r = 72;
+constexpr uint32_t kRegSoftmaxExact = 184, kRegDequantExact = 56, kRegIssueExact = 88;
 static_assert(2 * kRegSoftmaxKvi8r + kRegDequantKvi8r + kRegIssueKvi8r == 512, "register split");
 static_assert(2 * kRegSoftmaxExact + kRegDequantExact + kRegIssueExact == 512, "register split");
 
@@ -63,8 +60,7 @@ struct Smem {
   uint64_t q_full;
   uint64_t k_load[kNK], k_ready[kNK], k_free[kNK];
   uint64_t v_load[kNV], v_ready[kNV], v_free[kNV];
-  uint64_t s_full[kNQ][2], p_full[kNQ][2];  // per query tile and S buffer
-  uint64_t o_done[kNQ];                     // P.V of a sub-tile completed
+  uint64_t s_full[kNQ], p_full[kNQ];
   uint64_t o_full;
   uint64_t drain;
   uint32_t tmem_base;
@@ -164,28 +160,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = tid & 31;
   const int h = blockIdx.y;
   const int64_t row0 = a.q_begin + static_cast<int64_t>(blockIdx.x) * (kNQ * kBM);
-  const int n_tiles = static_cast<int>((a.kv_seq + kBN - 1) / kBN);   // staged 128-key tiles
-  const int n_sub = static_cast<int>((a.kv_seq + kSub - 1) / kSub);   // 64-key score sub-tiles
-  const int blk = a.kv_block_tiles * (kBN / kSub);                      // sub-tiles per kv_block
+  const int n_tiles = static_cast<int>((a.kv_seq + kBN - 1) / kBN);
+  const int blk = a.kv_block_tiles;
 
   if (tid == 0) {
     mbar_init(smem_u32(&sm.q_full), kKvi8r ? kNQ * kBM : 1);
     for (int s = 0; s < kNK; ++s) {
       mbar_init(smem_u32(&sm.k_load[s]), 1);
-      mbar_init(smem_u32(&sm.k_ready[s]), 128);
+      mbar_init(smem_u32(&sm.k_ready[s]), kWarpsPerGroup);
       mbar_init(smem_u32(&sm.k_free[s]), 1);
     }
     for (int s = 0; s < kNV; ++s) {
       mbar_init(smem_u32(&sm.v_load[s]), 1);
-      mbar_init(smem_u32(&sm.v_ready[s]), 128);
+      mbar_init(smem_u32(&sm.v_ready[s]), kWarpsPerGroup);
       mbar_init(smem_u32(&sm.v_free[s]), 1);
     }
     for (int q = 0; q < kNQ; ++q) {
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(smem_u32(&sm.s_full[q][b]), 1);
-        mbar_init(smem_u32(&sm.p_full[q][b]), kBM);
-      }
-      mbar_init(smem_u32(&sm.o_done[q]), 1);
+      mbar_init(smem_u32(&sm.s_full[q]), 1);
+      mbar_init(smem_u32(&sm.p_full[q]), kWarpsPerGroup);
     }
     mbar_init(smem_u32(&sm.o_full), 1);
     mbar_init(smem_u32(&sm.drain), 1);
@@ -246,42 +238,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_b = 0.f, l_b = 0.f;  // current block: running max (raw score units) and sum
     float M = 0.f, Lam = 0.f;    // blocks merged so far
     bool ok = true;
-    for (int t = 0; t < n_sub; ++t) {
-      const int sb = t & 1;  // S buffer of this sub-tile
-      if (!warp_wait(smem_u32(&sm.s_full[q][sb]), (t >> 1) & 1, wctx)) {
+    for (int j = 0; j < n_tiles; ++j) {
+      if (!warp_wait(smem_u32(&sm.s_full[q]), j & 1, wctx)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float s[64];
-      tmem_ld64(tS + sb * kSub, *reinterpret_cast<uint32_t(*)[64]>(s));
-      const int64_t valid = a.kv_seq - static_cast<int64_t>(t) * kSub;
-      if (valid < kSub) {
+      float s[128];
+      tmem_ld128(tS, *reinterpret_cast<uint32_t(*)[128]>(s));
+      const int64_t valid = a.kv_seq - static_cast<int64_t>(j) * kBN;
+      if (valid < kBN) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) s[c] = (c < valid) ? s[c] : -INFINITY;
+        for (int c = 0; c < 128; ++c) s[c] = (c < valid) ? s[c] : -INFINITY;
       }
       float mt;
       {
         float m4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-        for (int c = 4; c < 64; c += 8) {
+        for (int c = 4; c < 128; c += 8) {
 #pragma unroll
           for (int u = 0; u < 4; ++u) m4[u] = fmax3(m4[u], s[c + 2 * u], s[c + 2 * u + 1]);
         }
         mt = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
       }
 
-      if (t % blk == 0) {
-        if (t > 0) {
+      if (j % blk == 0) {
+        if (j > 0) {
           // merge the finished block (O_q, m_b, l_b) into (M, Lam, O row in
-          // global memory, rotated basis, un-normalised); O_q is final once
-          // the previous sub-tile's P.V has completed
-          if (!warp_wait(smem_u32(&sm.o_done[q]), (t - 1) & 1, wctx)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const bool first = (t / blk) == 1;
+          // global memory, rotated basis, un-normalised)
+          const bool first = (j / blk) == 1;
           float al = 0.f, be = 1.f;
           if (!first) {
             const float Mn = fmaxf(M, m_b);
@@ -319,12 +304,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         const bool need = (mt - m_b) * c2 > kLazyRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {
-          // O_q may only be touched once the previous sub-tile's P.V is done
-          if (!warp_wait(smem_u32(&sm.o_done[q]), (t - 1) & 1, wctx)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
           const float alpha = need ? ex2((m_b - mt) * c2) : 1.f;
           if (need) {
             l_b *= alpha;
@@ -342,24 +321,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       // p = 2^(s c - m c) in packed pairs, written as fp16 (bf16) pairs over
-      // the first 32 columns of this sub-tile's S buffer
+      // the first 64 columns of S
       const float2 cc = make_float2(c2, c2);
       const float2 nm = make_float2(-m_b * c2, -m_b * c2);
       float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-      uint32_t pk[32];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        float2 e = __ffma2_rn(make_float2(s[2 * k], s[2 * k + 1]), cc, nm);
-        e.x = ex2(e.x);
-        e.y = ex2(e.y);
-        if (k & 1) acc1 = __fadd2_rn(acc1, e);
-        else acc0 = __fadd2_rn(acc0, e);
-        pk[k] = pack2<kKvi8r>(e.x, e.y);
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int c = hlf * 64 + 2 * k;
+          float2 e = __ffma2_rn(make_float2(s[c], s[c + 1]), cc, nm);
+          e.x = ex2(e.x);
+          e.y = ex2(e.y);
+          if (k & 1) acc1 = __fadd2_rn(acc1, e);
+          else acc0 = __fadd2_rn(acc0, e);
+          pk[k] = pack2<kKvi8r>(e.x, e.y);
+        }
+        tmem_st32(tS + hlf * 32, pk);
       }
-      tmem_st32(tS + sb * kSub, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(smem_u32(&sm.p_full[q][sb]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[q]));
       const float2 acc = __fadd2_rn(acc0, acc1);
       l_b += acc.x + acc.y;
     }
@@ -371,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // free now: every MMA has completed and no copy is outstanding.
       tc_fence_after();
       uint8_t *stage = sm.k[0] + q * (kNQ * kTileBytes);
-      const int n_blocks = (n_sub + blk - 1) / blk;
+      const int n_blocks = (n_tiles + blk - 1) / blk;
       float ga, gb;
       if (n_blocks == 1) {
         ga = 0.f;
@@ -446,11 +430,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait(smem_u32(&sm.k_load[ks]), (j / kNK) & 1, wctx)) break;
         dequant_tile(sm.k[ks], sck, dw, lane);
         fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&sm.k_ready[ks]));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.k_ready[ks]));
         if (!warp_wait(smem_u32(&sm.v_load[vs]), (j / kNV) & 1, wctx)) break;
         dequant_tile(sm.v[vs], scv, dw, lane);
         fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&sm.v_ready[vs]));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.v_ready[vs]));
       }
     }
   } else {
@@ -514,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == 13 && lane == 0) {
       // ====================================================== MMA issuer
-      constexpr uint32_t idesc_qk = idesc_f16(!kKvi8r, false, kBM, kSub);
+      constexpr uint32_t idesc_qk = idesc_f16(!kKvi8r, false, kBM, kBN);
       constexpr uint32_t idesc_pv = idesc_f16(!kKvi8r, true, kBM, 128);
       uint64_t *k_rdy = kKvi8r ? sm.k_ready : sm.k_load;
       uint64_t *v_rdy = kKvi8r ? sm.v_ready : sm.v_load;
@@ -523,62 +509,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
       const uint64_t dk0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
       const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[0]), kChunkBytes, 1024);
-      // S_q[sb] = Q_q K^T over keys [64h, 64h+64) of staged K tile ks
-      auto issue_qk = [&](int q, int ks, int h, int sb) {
+      auto issue_qk = [&](int q, int ks) {
         const uint64_t dq = dq0 + static_cast<uint64_t>(q * (kTileBytes >> 4));
-        const uint64_t dk = dk0 + static_cast<uint64_t>((ks * kTileBytes + h * (kSub * 128)) >> 4);
+        const uint64_t dk = dk0 + static_cast<uint64_t>(ks * (kTileBytes >> 4));
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-          mma_ss(tmem + q * 128 + sb * kSub, dq + off, dk + off, idesc_qk, kk > 0);
+          mma_ss(tmem + q * 128, dq + off, dk + off, idesc_qk, kk > 0);
         }
       };
-      // O_q (+)= P_q[sb] V over keys [64h, 64h+64) of staged V tile vs
-      auto issue_pv = [&](int q, int vs, int h, int sb, bool acc) {
-        const uint64_t dv = dv0 + static_cast<uint64_t>((vs * kTileBytes + h * (kSub * 128)) >> 4);
+      auto issue_pv = [&](int q, int vs, bool acc) {
+        const uint64_t dv = dv0 + static_cast<uint64_t>(vs * (kTileBytes >> 4));
 #pragma unroll
-        for (int kk = 0; kk < kSub / 16; ++kk)
-          mma_ts(tmem + 256 + q * 128, tmem + q * 128 + sb * kSub + kk * 8, dv + (kk * 2048 >> 4), idesc_pv,
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + 256 + q * 128, tmem + q * 128 + kk * 8, dv + (kk * 2048 >> 4), idesc_pv,
                  (acc || kk > 0) ? 1u : 0u);
       };
-      // Issue order: QK(0), QK(1), then per sub-tile t: PV0(t), PV1(t),
-      // QK0(t+2), QK1(t+2).  S is double-buffered per query tile, so each
-      // softmax overlaps the next sub-tile's QK^T and the other tile's work.
       bool ok = mbar_wait(smem_u32(&sm.q_full), 0, wctx) && mbar_wait(smem_u32(&k_rdy[0]), 0, wctx);
       if (ok) {
         tc_fence_after();
-        for (int t0 = 0; t0 < 2 && t0 < n_sub; ++t0) {
-          issue_qk(0, 0, t0, t0);
-          mma_commit(smem_u32(&sm.s_full[0][t0]));
-          issue_qk(1, 0, t0, t0);
-          mma_commit(smem_u32(&sm.s_full[1][t0]));
-        }
+        issue_qk(0, 0);
+        mma_commit(smem_u32(&sm.s_full[0]));
+        issue_qk(1, 0);
+        mma_commit(smem_u32(&sm.s_full[1]));
         mma_commit(smem_u32(&sm.k_free[0]));
-        for (int t = 0; t < n_sub && ok; ++t) {
-          const int j = t >> 1, h = t & 1, sb = t & 1;
+        for (int j = 0; j < n_tiles && ok; ++j) {
           const int vs = j % kNV;
-          const bool acc = (t % blk) != 0;
-          if (h == 0 && !(ok = mbar_wait(smem_u32(&v_rdy[vs]), (j / kNV) & 1, wctx))) break;
-          for (int q = 0; q < kNQ; ++q) {
-            if (!(ok = mbar_wait(smem_u32(&sm.p_full[q][sb]), (t >> 1) & 1, wctx))) break;
-            tc_fence_after();
-            issue_pv(q, vs, h, sb, acc);
-            mma_commit(smem_u32(&sm.o_done[q]));
-          }
+          const bool acc = (j % blk) != 0;
+          const bool more = j + 1 < n_tiles;
+          const int ks1 = (j + 1) % kNK;
+          ok = mbar_wait(smem_u32(&v_rdy[vs]), (j / kNV) & 1, wctx) &&
+               mbar_wait(smem_u32(&sm.p_full[0]), j & 1, wctx);
           if (!ok) break;
-          if (h == 1 || t == n_sub - 1) mma_commit(smem_u32(&sm.v_free[vs]));
-          const int t2 = t + 2;
-          if (t2 < n_sub) {
-            const int j2 = t2 >> 1, h2 = t2 & 1, ks2 = j2 % kNK;
-            if (h2 == 0) {
-              if (!(ok = mbar_wait(smem_u32(&k_rdy[ks2]), (j2 / kNK) & 1, wctx))) break;
-              tc_fence_after();
-            }
-            issue_qk(0, ks2, h2, sb);
-            mma_commit(smem_u32(&sm.s_full[0][sb]));
-            issue_qk(1, ks2, h2, sb);
-            mma_commit(smem_u32(&sm.s_full[1][sb]));
-            if (h2 == 1 || t2 == n_sub - 1) mma_commit(smem_u32(&sm.k_free[ks2]));
+          tc_fence_after();
+          issue_pv(0, vs, acc);
+          if (more) {
+            if (!(ok = mbar_wait(smem_u32(&k_rdy[ks1]), ((j + 1) / kNK) & 1, wctx))) break;
+            tc_fence_after();
+            issue_qk(0, ks1);
+            mma_commit(smem_u32(&sm.s_full[0]));
+          }
+          if (!(ok = mbar_wait(smem_u32(&sm.p_full[1]), j & 1, wctx))) break;
+          tc_fence_after();
+          issue_pv(1, vs, acc);
+          mma_commit(smem_u32(&sm.v_free[vs]));
+          if (more) {
+            issue_qk(1, ks1);
+            mma_commit(smem_u32(&sm.s_full[1]));
+            mma_commit(smem_u32(&sm.k_free[ks1]));
           }
         }
         if (ok) mma_commit(smem_u32(&sm.o_full));
