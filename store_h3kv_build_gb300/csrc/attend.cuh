@@ -123,33 +123,22 @@ __device__ __forceinline__ void dequant_scales(const uint16_t *scales, int valid
 // in the second half of the tile buffer; on exit the whole buffer holds the
 // fp16 tile in the 128B-swizzled layout the MMA descriptors expect (two
 // 64-column halves of [128 rows x 128 bytes]).  Row r's codes share their
-// 128-byte slot with row r's fp16 columns 64-127.  Each warp owns 32 rows and
-// reads all of their codes before any of its lanes stores, so in place is
+// 128-byte slot with row r's fp16 columns 64-127, and every row is read by
+// one load instruction of its warp before any lane writes it, so in place is
 // safe.
 __device__ __forceinline__ void dequant_tile(uint8_t *tile, const uint16_t (&sc)[8], int dw, int lane) {
   const uint32_t g = dq_granule(lane);
-  uint8_t *half_base = tile + (g >> 2) * kChunkBytes;
-  const uint32_t G0 = (g & 3) * 2;
-  // two passes of 4 row groups: a pass loads all of its code granules before
-  // any of its stores (which overwrite those rows' codes in place), so no load
-  // is ever ordered after a store to the same rows
 #pragma unroll
-  for (int pass = 0; pass < 2; ++pass) {
-    uint4 raw[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      raw[u] = *reinterpret_cast<const uint4 *>(tile + kChunkBytes + dq_row(dw, pass * 4 + u, lane) * 128 + g * 16);
-    __syncwarp();
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int it = pass * 4 + u;
-      const uint32_t r = dq_row(dw, it, lane);
-      const __half s = __ushort_as_half(sc[it]);
-      uint32_t o[8];
-      dequant16(raw[u], __halves2half2(s, s), o);
-      *reinterpret_cast<uint4 *>(half_base + sw128_off(r, G0)) = make_uint4(o[0], o[1], o[2], o[3]);
-      *reinterpret_cast<uint4 *>(half_base + sw128_off(r, G0 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
-    }
+  for (int it = 0; it < 8; ++it) {
+    const uint32_t r = dq_row(dw, it, lane);
+    const uint4 raw = *reinterpret_cast<const uint4 *>(tile + kChunkBytes + r * 128 + g * 16);
+    const __half s = __ushort_as_half(sc[it]);
+    uint32_t o[8];
+    dequant16(raw, __halves2half2(s, s), o);
+    uint8_t *half_base = tile + (g >> 2) * kChunkBytes;
+    const uint32_t G0 = (g & 3) * 2;
+    *reinterpret_cast<uint4 *>(half_base + sw128_off(r, G0)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4 *>(half_base + sw128_off(r, G0 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
   }
 }
 
