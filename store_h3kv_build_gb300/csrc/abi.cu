@@ -278,7 +278,9 @@ h3kv_status h3kv_sync_status(void *stream) {
   if (word != 0) {
     if (cudaMemset(d->err, 0, sizeof(uint32_t)) != cudaSuccess) return H3KV_ERR_CUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return H3KV_ERR_CUDA;
-    return H3KV_ERR_DEVICE_TIMEOUT;
+    // bit 0: a bounded wait ran out; bit 1: the shared-memory base could not
+    // be aligned within the requested slack (the kernel returned at entry)
+    return (word & h3kv::kErrTimeout) ? H3KV_ERR_DEVICE_TIMEOUT : H3KV_ERR_CUDA;
   }
   return H3KV_OK;
 }

@@ -15,7 +15,7 @@ namespace h3kv {
 // code into the device error word and raises the CTA-local abort flag, so the
 // other roles stop issuing work and the CTA drains and exits.
 // ---------------------------------------------------------------------------
-enum : uint32_t { kErrTimeout = 1u };
+enum : uint32_t { kErrTimeout = 1u, kErrLayout = 2u };
 
 // Limit for the waits that drain a CTA's own copies and MMAs after an abort.
 // Those always complete within microseconds; the limit only guards exit.
