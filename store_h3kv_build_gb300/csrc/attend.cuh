@@ -265,20 +265,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t row = row0 + q * kBM + i;
         const bool row_ok = row < a.q_end;
         float *orow = a.o + (static_cast<int64_t>(h) * a.q_seq + (row_ok ? row : 0)) * 128 + wg * 64;
-        if (!warp_wait(smem_u32(&sm.s_full[q]), j & 1, wctx)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+        const bool got = warp_wait(smem_u32(&sm.s_full[q]), j & 1, wctx);
         float s[64];
-        tmem_ld64(tS, *reinterpret_cast<uint32_t(*)[64]>(s));
-        const int64_t valid = a.kv_seq - static_cast<int64_t>(j) * kBN - wg * 64;
-        if (valid < 64) {
+        float mp = -INFINITY;
+        if (got) {
+          tc_fence_after();
+          tmem_ld64(tS, *reinterpret_cast<uint32_t(*)[64]>(s));
+          const int64_t valid = a.kv_seq - static_cast<int64_t>(j) * kBN - wg * 64;
+          if (valid < 64) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) s[c] = (c < valid) ? s[c] : -INFINITY;
-        }
-        float mp;
-        {
+            for (int c = 0; c < 64; ++c) s[c] = (c < valid) ? s[c] : -INFINITY;
+          }
           float m4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
           for (int c = 4; c < 64; c += 8) {
@@ -287,10 +284,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mp = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
         }
-        // row max over both halves (the partner has also finished reading its
-        // S columns once it passes the barrier, so P may overwrite them)
+        // row max over both halves.  The barrier is an AND-reduction so that
+        // both warps of the pair stop together if either one's wait ran out
+        // (a plain barrier could otherwise wait for a warp that has left);
+        // once past it the partner has read its S columns, so P may overwrite.
         sm.red[q][wg][i] = mp;
-        named_bar_sync(pair_bar, 64);
+        if (!named_bar_and(pair_bar, 64, got)) {
+          ok = false;
+          break;
+        }
         const float mt = fmaxf(mp, sm.red[q][wg ^ 1][i]);
 
         if (j % blk == 0) {
@@ -375,7 +377,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
 
-    if (ok && warp_wait(smem_u32(&sm.o_full), 0, wctx)) {
+    bool fin = ok && warp_wait(smem_u32(&sm.o_full), 0, wctx);
+    // the epilogue syncs the pair, so both warps must agree to enter it
+    fin = named_bar_and(pair_bar, 64, fin);
+    if (fin) {
       tc_fence_after();
       const int n_blocks = (n_tiles + blk - 1) / blk;
 #pragma unroll
