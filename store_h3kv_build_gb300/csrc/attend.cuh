@@ -48,8 +48,8 @@ constexpr float kLazyRescaleLog2 = 8.0f;    // rescale O only when the max grows
 // Register split per warpgroup (setmaxnreg).  The launch gives every thread
 // 128 (512 threads x 128 = the 64K register file); each split below sums to
 // the same total: 128 x (2 x softmax + dequant + issue) = 65536.
-constexpr uint32_t kRegSoftmaxKvi8r = 168, kRegDequantKvi8r = 72, kRegIssueKvi8r = 104;
-constexpr uint32_t kRegSoftmaxExact = 160, kRegDequantExact = 64, kRegIssueExact = 128;
+constexpr uint32_t kRegSoftmaxKvi8r = 184, kRegDequantKvi8r = 72, kRegIssueKvi8r = 72;
+constexpr uint32_t kRegSoftmaxExact = 184, kRegDequantExact = 56, kRegIssueExact = 88;
 static_assert(2 * kRegSoftmaxKvi8r + kRegDequantKvi8r + kRegIssueKvi8r == 512, "register split");
 static_assert(2 * kRegSoftmaxExact + kRegDequantExact + kRegIssueExact == 512, "register split");
 
@@ -61,20 +61,14 @@ struct Smem {
   uint64_t k_load[kNK], k_ready[kNK], k_free[kNK];
   uint64_t v_load[kNV], v_ready[kNV], v_free[kNV];
   uint64_t s_full[kNQ], p_full[kNQ];
-  float red[kNQ][2][kBM];  // row maxima / denominators exchanged between the two column halves
   uint64_t o_full;
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
 
-// Dynamic shared memory is requested with this much slack for aligning the
-// tiles to 1024 bytes (the 128-byte swizzle atom); the kernel checks the base
-// it gets and refuses (error word, early return) if the slack is not enough.
-constexpr uint32_t kMaxSmem = 232448;
-constexpr uint32_t kPadBudget = (kMaxSmem - sizeof(Smem)) & ~15u;
-constexpr size_t kSmemBytes = sizeof(Smem) + kPadBudget;
-static_assert(sizeof(Smem) + 64 <= kMaxSmem, "shared memory budget");
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx &w) {
   const bool ok = mbar_wait(bar, parity, w);
@@ -159,13 +153,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  {
-    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
-    if (pad > kPadBudget) {  // uniform across the CTA: nothing has started yet
-      if (threadIdx.x == 0) atomicOr(a.err, kErrLayout);
-      return;
-    }
-  }
   Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int tid = threadIdx.x;
@@ -190,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int q = 0; q < kNQ; ++q) {
       mbar_init(smem_u32(&sm.s_full[q]), 1);
-      mbar_init(smem_u32(&sm.p_full[q]), 2 * kWarpsPerGroup);
+      mbar_init(smem_u32(&sm.p_full[q]), kWarpsPerGroup);
     }
     mbar_init(smem_u32(&sm.o_full), 1);
     mbar_init(smem_u32(&sm.drain), 1);
@@ -209,29 +196,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 8) {
     // =================================================== softmax warpgroups
-    // Column-split softmax: both warpgroups work on every query tile, warpgroup
-    // wg on key columns [64 wg, 64 wg + 64) of each 128-key tile, so the
-    // critical path of one tile's softmax is half a row per thread.  Thread
-    // (wq, lane) owns row i = 32 wq + lane (its TMEM lane) of both query tiles.
-    // Warp wq of each warpgroup forms a pair that exchanges the row maxima
-    // through shared memory behind named barrier 1 + wq; both halves of a row
-    // then use one max, and their partial row sums add up at the end.
     reg_alloc<kKvi8r ? kRegSoftmaxKvi8r : kRegSoftmaxExact>();
-    const int wg = warp >> 2;
-    const int wq = warp & 3;
-    const uint32_t i = wq * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t pair_bar = 1 + wq;
+    const int q = warp >> 2;
+    const uint32_t i = tid & 127;  // row in the query tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + q * 128;
+    const uint32_t tO = tmem + lane_base + 256 + q * 128;
+    const int64_t row = row0 + q * kBM + i;
+    const bool row_ok = row < a.q_end;
+    float *orow = a.o + (static_cast<int64_t>(h) * a.q_seq + (row_ok ? row : 0)) * 128;
     const float c2 = a.scale_log2;
 
     if constexpr (kKvi8r) {
-      // q' = fp16(q H): warpgroup wg rotates query tile wg, each warp its 32
-      // rows one at a time across the warp (lane l holds elements 4l..4l+3),
-      // written in the 128B-swizzled K-major layout of the MMA's A operand.
+      // q' = fp16(q H): each warp rotates its 32 rows of the query tile, one
+      // row at a time across the warp (lane l holds elements 4l..4l+3), and
+      // writes them in the 128B-swizzled K-major layout of the MMA's A operand.
+      const int wq = warp & 3;
       uint2 buf[32];
 #pragma unroll
       for (int rr = 0; rr < 32; ++rr) {
-        const int64_t r = row0 + wg * kBM + wq * 32 + rr;
+        const int64_t r = row0 + q * kBM + wq * 32 + rr;
         buf[rr] = r < a.q_end ? *reinterpret_cast<const uint2 *>(a.q + (static_cast<int64_t>(h) * a.q_seq + r) * 128 +
                                                                   4 * lane)
                               : make_uint2(0u, 0u);
@@ -244,216 +228,188 @@ __global__ void __launch_bounds__(kThreads, 1)
         fwht128_warp(x, lane);
         const uint2 w = make_uint2(pack_f16x2(x[0] * kInvSqrt128, x[1] * kInvSqrt128),
                                    pack_f16x2(x[2] * kInvSqrt128, x[3] * kInvSqrt128));
-        *reinterpret_cast<uint2 *>(sm.q[wg] + (lane >> 4) * kChunkBytes + sw128_off(ti, (lane & 15) >> 1) +
+        *reinterpret_cast<uint2 *>(sm.q[q] + (lane >> 4) * kChunkBytes + sw128_off(ti, (lane & 15) >> 1) +
                                    (lane & 1) * 8) = w;
       }
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&sm.q_full));
     }
 
-    // per query tile: running max of the current block (raw score units) and
-    // this thread's partial sum; the merged blocks' max and partial sum
-    float m_b[kNQ] = {0.f, 0.f}, l_b[kNQ] = {0.f, 0.f};
-    float M[kNQ] = {0.f, 0.f}, Lam[kNQ] = {0.f, 0.f};
+    float m_b = 0.f, l_b = 0.f;  // current block: running max (raw score units) and sum
+    float M = 0.f, Lam = 0.f;    // blocks merged so far
     bool ok = true;
-    for (int j = 0; j < n_tiles && ok; ++j) {
+    for (int j = 0; j < n_tiles; ++j) {
+      if (!warp_wait(smem_u32(&sm.s_full[q]), j & 1, wctx)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[128];
+      tmem_ld128(tS, *reinterpret_cast<uint32_t(*)[128]>(s));
+      const int64_t valid = a.kv_seq - static_cast<int64_t>(j) * kBN;
+      if (valid < kBN) {
 #pragma unroll
-      for (int q = 0; q < kNQ; ++q) {
-        const uint32_t tS = tmem + lane_base + q * 128 + wg * 64;        // my 64 score columns
-        const uint32_t tP = tmem + lane_base + q * 128 + wg * 32;        // my 64 keys of P (fp16 pairs)
-        const uint32_t tO = tmem + lane_base + 256 + q * 128 + wg * 64;  // my 64 output columns
-        const int64_t row = row0 + q * kBM + i;
-        const bool row_ok = row < a.q_end;
-        float *orow = a.o + (static_cast<int64_t>(h) * a.q_seq + (row_ok ? row : 0)) * 128 + wg * 64;
-        const bool got = warp_wait(smem_u32(&sm.s_full[q]), j & 1, wctx);
-        float s[64];
-        float mp = -INFINITY;
-        if (got) {
-          tc_fence_after();
-          tmem_ld64(tS, *reinterpret_cast<uint32_t(*)[64]>(s));
-          const int64_t valid = a.kv_seq - static_cast<int64_t>(j) * kBN - wg * 64;
-          if (valid < 64) {
+        for (int c = 0; c < 128; ++c) s[c] = (c < valid) ? s[c] : -INFINITY;
+      }
+      float mt;
+      {
+        float m4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-            for (int c = 0; c < 64; ++c) s[c] = (c < valid) ? s[c] : -INFINITY;
-          }
-          float m4[4] = {s[0], s[1], s[2], s[3]};
+        for (int c = 4; c < 128; c += 8) {
 #pragma unroll
-          for (int c = 4; c < 64; c += 8) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) m4[u] = fmax3(m4[u], s[c + 2 * u], s[c + 2 * u + 1]);
-          }
-          mp = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+          for (int u = 0; u < 4; ++u) m4[u] = fmax3(m4[u], s[c + 2 * u], s[c + 2 * u + 1]);
         }
-        // row max over both halves.  The barrier is an AND-reduction so that
-        // both warps of the pair stop together if either one's wait ran out
-        // (a plain barrier could otherwise wait for a warp that has left);
-        // once past it the partner has read its S columns, so P may overwrite.
-        sm.red[q][wg][i] = mp;
-        if (!named_bar_and(pair_bar, 64, got)) {
-          ok = false;
-          break;
-        }
-        const float mt = fmaxf(mp, sm.red[q][wg ^ 1][i]);
+        mt = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+      }
 
-        if (j % blk == 0) {
-          if (j > 0) {
-            // merge the finished block (O_q, m_b, l_b) into (M, Lam, O row in
-            // global memory, rotated basis, un-normalised), my 64 columns
-            const bool first = (j / blk) == 1;
-            float al = 0.f, be = 1.f;
-            if (!first) {
-              const float Mn = fmaxf(M[q], m_b[q]);
-              al = ex2((M[q] - Mn) * c2);
-              be = ex2((m_b[q] - Mn) * c2);
-              Lam[q] = Lam[q] * al + l_b[q] * be;
-              M[q] = Mn;
-            } else {
-              M[q] = m_b[q];
-              Lam[q] = l_b[q];
-            }
+      if (j % blk == 0) {
+        if (j > 0) {
+          // merge the finished block (O_q, m_b, l_b) into (M, Lam, O row in
+          // global memory, rotated basis, un-normalised)
+          const bool first = (j / blk) == 1;
+          float al = 0.f, be = 1.f;
+          if (!first) {
+            const float Mn = fmaxf(M, m_b);
+            al = ex2((M - Mn) * c2);
+            be = ex2((m_b - Mn) * c2);
+            Lam = Lam * al + l_b * be;
+            M = Mn;
+          } else {
+            M = m_b;
+            Lam = l_b;
+          }
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-              float o[16];
-              tmem_ld16(tO + c * 16, *reinterpret_cast<uint32_t(*)[16]>(o));
-              if (row_ok) {
-                float4 *dst = reinterpret_cast<float4 *>(orow + c * 16);
+          for (int c = 0; c < 8; ++c) {
+            float o[16];
+            tmem_ld16(tO + c * 16, *reinterpret_cast<uint32_t(*)[16]>(o));
+            if (row_ok) {
+              float4 *dst = reinterpret_cast<float4 *>(orow + c * 16);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  float4 v = make_float4(o[4 * k] * be, o[4 * k + 1] * be, o[4 * k + 2] * be, o[4 * k + 3] * be);
-                  if (!first) {
-                    const float4 g = dst[k];
-                    v.x = fmaf(g.x, al, v.x);
-                    v.y = fmaf(g.y, al, v.y);
-                    v.z = fmaf(g.z, al, v.z);
-                    v.w = fmaf(g.w, al, v.w);
-                  }
-                  dst[k] = v;
+              for (int k = 0; k < 4; ++k) {
+                float4 v = make_float4(o[4 * k] * be, o[4 * k + 1] * be, o[4 * k + 2] * be, o[4 * k + 3] * be);
+                if (!first) {
+                  const float4 g = dst[k];
+                  v.x = fmaf(g.x, al, v.x);
+                  v.y = fmaf(g.y, al, v.y);
+                  v.z = fmaf(g.z, al, v.z);
+                  v.w = fmaf(g.w, al, v.w);
                 }
+                dst[k] = v;
               }
             }
           }
-          m_b[q] = mt;
-          l_b[q] = 0.f;
-        } else {
-          const bool need = (mt - m_b[q]) * c2 > kLazyRescaleLog2;
-          if (__any_sync(0xffffffffu, need)) {
-            const float alpha = need ? ex2((m_b[q] - mt) * c2) : 1.f;
-            if (need) {
-              l_b[q] *= alpha;
-              m_b[q] = mt;
-            }
+        }
+        m_b = mt;
+        l_b = 0.f;
+      } else {
+        const bool need = (mt - m_b) * c2 > kLazyRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? ex2((m_b - mt) * c2) : 1.f;
+          if (need) {
+            l_b *= alpha;
+            m_b = mt;
+          }
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-              uint32_t o[16];
-              tmem_ld16(tO + c * 16, o);
+          for (int c = 0; c < 8; ++c) {
+            uint32_t o[16];
+            tmem_ld16(tO + c * 16, o);
 #pragma unroll
-              for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-              tmem_st16(tO + c * 16, o);
-            }
+            for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            tmem_st16(tO + c * 16, o);
           }
         }
+      }
 
-        // p = 2^(s c - m c) in packed pairs, written as fp16 (bf16) pairs
-        const float2 cc = make_float2(c2, c2);
-        const float2 nm = make_float2(-m_b[q] * c2, -m_b[q] * c2);
-        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+      // p = 2^(s c - m c) in packed pairs, written as fp16 (bf16) pairs over
+      // the first 64 columns of S
+      const float2 cc = make_float2(c2, c2);
+      const float2 nm = make_float2(-m_b * c2, -m_b * c2);
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) {
         uint32_t pk[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          float2 e = __ffma2_rn(make_float2(s[2 * k], s[2 * k + 1]), cc, nm);
+          const int c = hlf * 64 + 2 * k;
+          float2 e = __ffma2_rn(make_float2(s[c], s[c + 1]), cc, nm);
           e.x = ex2(e.x);
           e.y = ex2(e.y);
           if (k & 1) acc1 = __fadd2_rn(acc1, e);
           else acc0 = __fadd2_rn(acc0, e);
           pk[k] = pack2<kKvi8r>(e.x, e.y);
         }
-        tmem_st32(tP, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[q]));
-        const float2 acc = __fadd2_rn(acc0, acc1);
-        l_b[q] += acc.x + acc.y;
+        tmem_st32(tS + hlf * 32, pk);
       }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[q]));
+      const float2 acc = __fadd2_rn(acc0, acc1);
+      l_b += acc.x + acc.y;
     }
 
-    bool fin = ok && warp_wait(smem_u32(&sm.o_full), 0, wctx);
-    // the epilogue syncs the pair, so both warps must agree to enter it
-    fin = named_bar_and(pair_bar, 64, fin);
-    if (fin) {
+    if (ok && warp_wait(smem_u32(&sm.o_full), 0, wctx)) {
+      // epilogue, phase 1: each thread finishes its own row (final block
+      // merge, 1/Lambda) and stages it in shared memory, fp32, with 16-byte
+      // granule gi of row i at position gi ^ (i mod 32).  The K/V rings are
+      // free now: every MMA has completed and no copy is outstanding.
       tc_fence_after();
+      uint8_t *stage = sm.k[0] + q * (kNQ * kTileBytes);
       const int n_blocks = (n_tiles + blk - 1) / blk;
+      float ga, gb;
+      if (n_blocks == 1) {
+        ga = 0.f;
+        gb = 1.f / l_b;
+      } else {
+        const float Mn = fmaxf(M, m_b);
+        const float al = ex2((M - Mn) * c2);
+        const float be = ex2((m_b - Mn) * c2);
+        const float inv = 1.f / (Lam * al + l_b * be);
+        ga = al * inv;
+        gb = be * inv;
+      }
 #pragma unroll
-      for (int q = 0; q < kNQ; ++q) {
-        const uint32_t tO = tmem + lane_base + 256 + q * 128 + wg * 64;
-        const int64_t row = row0 + q * kBM + i;
-        const bool row_ok = row < a.q_end;
-        float *orow = a.o + (static_cast<int64_t>(h) * a.q_seq + (row_ok ? row : 0)) * 128 + wg * 64;
-        // final merge weights (identical in both halves of the row) and the
-        // row's total denominator from the two partial sums
-        float ga, gb, den;
-        if (n_blocks == 1) {
-          ga = 0.f;
-          gb = 1.f;
-          den = l_b[q];
-        } else {
-          const float Mn = fmaxf(M[q], m_b[q]);
-          ga = ex2((M[q] - Mn) * c2);
-          gb = ex2((m_b[q] - Mn) * c2);
-          den = Lam[q] * ga + l_b[q] * gb;
-        }
-        sm.red[q][wg][i] = den;
-        named_bar_sync(pair_bar, 64);
-        const float inv = 1.f / (den + sm.red[q][wg ^ 1][i]);
-        ga *= inv;
-        gb *= inv;
-        // phase 1: my 64 finished columns into shared staging (fp32, 16-byte
-        // granule gi of row i at position gi ^ (i mod 32)); the K/V rings are
-        // free now (every MMA has completed, no copy is outstanding)
-        uint8_t *stage = sm.k[0] + q * (kNQ * kTileBytes);
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float o[16];
-          tmem_ld16(tO + c * 16, *reinterpret_cast<uint32_t(*)[16]>(o));
+      for (int c = 0; c < 4; ++c) {
+        float o[32];
+        tmem_ld32(tO + c * 32, *reinterpret_cast<uint32_t(*)[32]>(o));
 #pragma unroll
-          for (int k = 0; k < 16; ++k) o[k] *= gb;
-          if (n_blocks > 1 && row_ok) {
-            const float4 *src = reinterpret_cast<const float4 *>(orow + c * 16);
+        for (int k = 0; k < 32; ++k) o[k] *= gb;
+        if (n_blocks > 1 && row_ok) {
+          const float4 *src = reinterpret_cast<const float4 *>(orow + c * 32);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float4 g = src[k];
-              o[4 * k + 0] = fmaf(g.x, ga, o[4 * k + 0]);
-              o[4 * k + 1] = fmaf(g.y, ga, o[4 * k + 1]);
-              o[4 * k + 2] = fmaf(g.z, ga, o[4 * k + 2]);
-              o[4 * k + 3] = fmaf(g.w, ga, o[4 * k + 3]);
-            }
-          }
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t gi = wg * 16 + c * 4 + k;
-            *reinterpret_cast<float4 *>(stage + i * 512 + ((gi ^ (i & 31)) << 4)) =
-                make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+          for (int k = 0; k < 8; ++k) {
+            const float4 g = src[k];
+            o[4 * k + 0] = fmaf(g.x, ga, o[4 * k + 0]);
+            o[4 * k + 1] = fmaf(g.y, ga, o[4 * k + 1]);
+            o[4 * k + 2] = fmaf(g.z, ga, o[4 * k + 2]);
+            o[4 * k + 3] = fmaf(g.w, ga, o[4 * k + 3]);
           }
         }
-        named_bar_sync(pair_bar, 64);
-        // phase 2: the pair splits its 32 rows; each warp takes 16 rows one at
-        // a time across the warp: un-rotate (kvi8r: O = O' H^T) and store
-        // coalesced
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t gi = c * 8 + k;
+          *reinterpret_cast<float4 *>(stage + i * 512 + ((gi ^ (i & 31)) << 4)) =
+              make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+        }
+      }
+      __syncwarp();
+      // phase 2: each warp takes its 32 rows one at a time across the warp:
+      // un-rotate (kvi8r: O = O' H^T, H symmetric) and store coalesced.
+      const int wq = warp & 3;
 #pragma unroll 4
-        for (int rr = 0; rr < 16; ++rr) {
-          const uint32_t ti = wq * 32 + wg * 16 + rr;
-          const float4 v = *reinterpret_cast<const float4 *>(stage + ti * 512 + ((lane ^ (ti & 31)) << 4));
-          float x[4] = {v.x, v.y, v.z, v.w};
-          if constexpr (kKvi8r) {
-            fwht128_warp(x, lane);
+      for (int rr = 0; rr < 32; ++rr) {
+        const uint32_t ti = wq * 32 + rr;
+        const float4 v = *reinterpret_cast<const float4 *>(stage + ti * 512 + ((lane ^ (ti & 31)) << 4));
+        float x[4] = {v.x, v.y, v.z, v.w};
+        if constexpr (kKvi8r) {
+          fwht128_warp(x, lane);
 #pragma unroll
-            for (int t = 0; t < 4; ++t) x[t] *= kInvSqrt128;
-          }
-          const int64_t r = row0 + q * kBM + ti;
-          if (r < a.q_end)
-            *reinterpret_cast<float4 *>(a.o + (static_cast<int64_t>(h) * a.q_seq + r) * 128 + 4 * lane) =
-                make_float4(x[0], x[1], x[2], x[3]);
+          for (int t = 0; t < 4; ++t) x[t] *= kInvSqrt128;
         }
+        const int64_t r = row0 + q * kBM + ti;
+        if (r < a.q_end)
+          *reinterpret_cast<float4 *>(a.o + (static_cast<int64_t>(h) * a.q_seq + r) * 128 + 4 * lane) =
+              make_float4(x[0], x[1], x[2], x[3]);
       }
     }
   } else if (warp < 12) {
