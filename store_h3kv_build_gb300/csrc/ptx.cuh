@@ -386,6 +386,35 @@ __device__ __forceinline__ void fwht128(float (&x)[128]) {
   }
 }
 
+// Same transform with the butterflies of strides 2 .. 64 done two at a time
+// in packed fp32 (a + b with one add, a - b as fma(b, -1, a), both exactly
+// rounded, so the result is bit-identical to the scalar version).
+__device__ __forceinline__ void fwht128_packed(float (&x)[128]) {
+#pragma unroll
+  for (int i = 0; i < 128; i += 2) {
+    const float a = x[i], b = x[i + 1];
+    x[i] = a + b;
+    x[i + 1] = a - b;
+  }
+  const float2 neg1 = make_float2(-1.f, -1.f);
+#pragma unroll
+  for (int h = 2; h < 128; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 128; i += 2) {
+      if ((i & h) == 0) {
+        const float2 a = make_float2(x[i], x[i + 1]);
+        const float2 b = make_float2(x[i + h], x[i + h + 1]);
+        const float2 sum = __fadd2_rn(a, b);
+        const float2 dif = __ffma2_rn(b, neg1, a);
+        x[i] = sum.x;
+        x[i + 1] = sum.y;
+        x[i + h] = dif.x;
+        x[i + h + 1] = dif.y;
+      }
+    }
+  }
+}
+
 // Warp-cooperative version: lane l holds elements 4l .. 4l+3 of one
 // 128-vector.  Stages of stride 1 and 2 run in-lane, strides 4 .. 64 pair
 // lanes l and l ^ (stride / 4) through shuffles.

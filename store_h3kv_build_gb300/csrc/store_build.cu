@@ -121,11 +121,15 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       mbar_arrive(smem_u32(&sm.empty[s]));
 
-      fwht128(x);  // x now holds sqrt(128) * (row H)
+      fwht128_packed(x);  // x now holds sqrt(128) * (row H)
 
-      float amax = 0.f;
+      float am[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int e = 0; e < 128; ++e) amax = fmaxf(amax, fabsf(x[e]));
+      for (int e = 0; e < 128; e += 8) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) am[u] = fmax3(am[u], fabsf(x[e + 2 * u]), fabsf(x[e + 2 * u + 1]));
+      }
+      const float amax = fmax3(am[0], am[1], fmaxf(am[2], am[3]));
       // s = fp16(absmax(x H) / 127), saturated at the largest finite fp16
       const float a = amax * kInvSqrt128;
       __half sh = __float2half_rn(__fdiv_rn(a, 127.0f));
@@ -149,11 +153,19 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           uint32_t q[4];
+          const int e = g * 16 + k * 4;
+          if (!clamp) {
+            const float2 mm = make_float2(m, m), mg = make_float2(kMagic, kMagic);
+            const float2 lo = __ffma2_rn(make_float2(x[e], x[e + 1]), mm, mg);
+            const float2 hi = __ffma2_rn(make_float2(x[e + 2], x[e + 3]), mm, mg);
+            q[0] = __float_as_uint(lo.x);
+            q[1] = __float_as_uint(lo.y);
+            q[2] = __float_as_uint(hi.x);
+            q[3] = __float_as_uint(hi.y);
+          } else {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float v = x[g * 16 + k * 4 + u];
-            q[u] = clamp ? __float_as_uint(fminf(fmaxf(v * m, -127.f), 127.f) + kMagic)
-                         : __float_as_uint(fmaf(v, m, kMagic));
+            for (int u = 0; u < 4; ++u)
+              q[u] = __float_as_uint(fminf(fmaxf(x[e + u] * m, -127.f), 127.f) + kMagic);
           }
           const uint32_t lo = __byte_perm(q[0], q[1], 0x0040);
           const uint32_t hi = __byte_perm(q[2], q[3], 0x0040);
