@@ -92,12 +92,24 @@ class Store:
         self.heads, self.seq = int(k_codes.shape[0]), int(k_codes.shape[1])
 
     @classmethod
-    def empty(cls, heads: int, seq: int, device="cuda") -> "Store":
-        kc = torch.empty((heads, seq, HEAD_DIM), dtype=torch.int8, device=device)
+    def empty(cls, heads: int, seq: int, device="cuda", host: bool = False) -> "Store":
+        """Uninitialised store buffers.  ``host=True`` places them in pinned
+        host memory: on a Grace-Blackwell node the kernels read (and the
+        store build writes) them directly over NVLink-C2C, so the whole
+        sequence's K/V need not occupy HBM."""
+        if host:
+            kw = dict(pin_memory=True)
+        else:
+            kw = dict(device=device)
+        kc = torch.empty((heads, seq, HEAD_DIM), dtype=torch.int8, **kw)
         vc = torch.empty_like(kc)
-        ks = torch.empty((heads, seq), dtype=torch.float16, device=device)
+        ks = torch.empty((heads, seq), dtype=torch.float16, **kw)
         vs = torch.empty_like(ks)
         return cls(kc, vc, ks, vs)
+
+    @property
+    def in_host_memory(self) -> bool:
+        return not self.k_codes.is_cuda
 
     def c_struct(self) -> h3kv_store:
         return h3kv_store(_ptr(self.k_codes), _ptr(self.v_codes), _ptr(self.k_scales), _ptr(self.v_scales),
