@@ -112,6 +112,29 @@ h3kv_status h3kv_attend_exact(const uint16_t *Q, int64_t q_seq, const uint16_t *
                               int32_t heads, int64_t kv_seq, int32_t head_dim, int32_t q_chunk,
                               int32_t kv_block, float softmax_scale, float *O, void *stream);
 
+/* Device bytes of the staging buffer h3kv_attend_staged needs: one kv_block
+ * of codes and scales of K and V for every head, 2 * heads * kv_block * 130
+ * (kv_block = 0 means 16384).  Returns 0 for invalid arguments. */
+size_t h3kv_staging_bytes(int32_t heads, int32_t kv_block);
+
+/* kvi8r attention over a store that lives outside HBM -- e.g. in pinned
+ * Grace memory -- staged through HBM one kv_block at a time: the "host-staged
+ * K/V design" the kv_block row of the H3 Streamed Blocks Inputs table keeps
+ * the blockwise combine for.  For each block (in order) the block's codes and
+ * scales of every head are copied into `staging` (device memory,
+ * >= h3kv_staging_bytes(store->heads, kv_block)) and every query chunk
+ * attends over it; the log-sum-exp combine across blocks is carried by
+ * `state` (device fp32 [store->heads, q_seq, 2]: running max and sum per
+ * query row) with O itself as the running un-normalised output.  The result
+ * is bit-identical to h3kv_attend on the same store, q_chunk and kv_block.
+ * Arguments otherwise as h3kv_attend; `store` may point to host (pinned for
+ * asynchronous copies) or device memory.  The library allocates nothing:
+ * staging and state are caller-owned scratch, reused by each call, so calls
+ * that overlap on the GPU must not share them. */
+h3kv_status h3kv_attend_staged(const uint16_t *Q, int64_t q_seq, const h3kv_store *store, int32_t q_chunk,
+                               int32_t kv_block, float softmax_scale, float *O, void *staging,
+                               size_t staging_bytes, float *state, void *stream);
+
 /* Synchronise `stream`, then return and clear the device error word that the
  * kernels set when a bounded wait runs out (H3KV_ERR_DEVICE_TIMEOUT), or
  * H3KV_ERR_CUDA if the synchronisation itself reports an error. */

@@ -49,6 +49,9 @@ _SIGS = {
     "h3kv_attend": (ctypes.c_int, [_vp, _i64, ctypes.POINTER(h3kv_store), _i32, _i32, _f32, _vp, _vp]),
     "h3kv_attend_exact": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _f32, _vp, _vp]),
     "h3kv_sync_status": (ctypes.c_int, [_vp]),
+    "h3kv_staging_bytes": (ctypes.c_size_t, [_i32, _i32]),
+    "h3kv_attend_staged": (ctypes.c_int, [_vp, _i64, ctypes.POINTER(h3kv_store), _i32, _i32, _f32, _vp, _vp,
+                                          ctypes.c_size_t, _vp, _vp]),
     "h3kv_set_wait_timeout_ns": (ctypes.c_int, [ctypes.c_uint64]),
     "h3kv_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _vp]),
     "h3kv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -138,6 +141,29 @@ def attend(Q: torch.Tensor, store: Store, q_chunk: int = 16384, kv_block: int = 
     st = store.c_struct()
     check(h3kv_attend(_ptr(Q), q_seq, ctypes.byref(st), int(q_chunk), int(kv_block), float(softmax_scale),
                       _ptr(out), _stream(stream)), "h3kv_attend")
+    return out
+
+
+def attend_staged(Q: torch.Tensor, store: Store, q_chunk: int = 16384, kv_block: int = 0,
+                  softmax_scale: float = 0.0, out: torch.Tensor | None = None, staging: torch.Tensor | None = None,
+                  state: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """h3kv_attend_staged: kvi8r attention over a store held outside HBM (e.g.
+    ``Store.empty(..., host=True)``), staged through HBM one kv_block at a
+    time.  ``staging`` (uint8, >= h3kv_staging_bytes) and ``state`` (fp32
+    [heads, q_seq, 2]) are device scratch; they are created here if not
+    given."""
+    dev = Q.device
+    heads, q_seq = int(Q.shape[0]), int(Q.shape[1])
+    out = torch.empty(Q.shape, dtype=torch.float32, device=dev) if out is None else out
+    nbytes = int(h3kv_staging_bytes(store.heads, int(kv_block)))
+    if staging is None:
+        staging = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    if state is None:
+        state = torch.empty((heads, q_seq, 2), dtype=torch.float32, device=dev)
+    st = store.c_struct()
+    check(h3kv_attend_staged(_ptr(Q), q_seq, ctypes.byref(st), int(q_chunk), int(kv_block), float(softmax_scale),
+                             _ptr(out), _ptr(staging), staging.numel() * staging.element_size(), _ptr(state),
+                             _stream(stream)), "h3kv_attend_staged")
     return out
 
 

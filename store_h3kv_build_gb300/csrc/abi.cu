@@ -200,6 +200,7 @@ h3kv_status h3kv_attend(const uint16_t *Q, int64_t q_seq, const h3kv_store *stor
   a.o = O;
   a.q_seq = q_seq;
   a.kv_seq = store->seq;
+  a.kv_stride = store->seq;
   a.heads = store->heads;
   a.kv_block_tiles = kvb / H3KV_KV_TILE;
   a.scale_log2 = scale_log2_of(softmax_scale);
@@ -240,6 +241,7 @@ h3kv_status h3kv_attend_exact(const uint16_t *Q, int64_t q_seq, const uint16_t *
   a.o = O;
   a.q_seq = q_seq;
   a.kv_seq = kv_seq;
+  a.kv_stride = kv_seq;
   a.heads = heads;
   a.kv_block_tiles = kv_block == 0 ? static_cast<int32_t>(n_tiles) : kv_block / H3KV_KV_TILE;
   a.scale_log2 = scale_log2_of(softmax_scale);
@@ -250,6 +252,79 @@ h3kv_status h3kv_attend_exact(const uint16_t *Q, int64_t q_seq, const uint16_t *
     a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
     if (h3kv::launch_attend_exact(tq, tk, tv, a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return H3KV_ERR_CUDA;
+  }
+  return H3KV_OK;
+}
+
+size_t h3kv_staging_bytes(int32_t heads, int32_t kv_block) {
+  if (heads < 0 || kv_block < 0 || kv_block % H3KV_KV_TILE != 0) return 0;
+  const size_t kvb = static_cast<size_t>(kv_block == 0 ? H3KV_DEFAULT_KV_BLOCK : kv_block);
+  return 2 * static_cast<size_t>(heads) * kvb * (H3KV_HEAD_DIM + 2);
+}
+
+h3kv_status h3kv_attend_staged(const uint16_t *Q, int64_t q_seq, const h3kv_store *store, int32_t q_chunk,
+                               int32_t kv_block, float softmax_scale, float *O, void *staging,
+                               size_t staging_bytes, float *state, void *stream) {
+  if (!store || q_seq < 0 || store->heads < 0 || store->seq < 0) return H3KV_ERR_INVALID_ARG;
+  if (store->head_dim != H3KV_HEAD_DIM) return H3KV_ERR_UNSUPPORTED;
+  h3kv_status st = check_chunks(q_chunk, kv_block);
+  if (st != H3KV_OK) return st;
+  if (store->heads == 0 || q_seq == 0) return H3KV_OK;
+  if (store->seq == 0) return H3KV_ERR_INVALID_ARG;
+  const int64_t H = store->heads;
+  if (H * q_seq > kMaxRows || H * store->seq > kMaxRows) return H3KV_ERR_INVALID_ARG;
+  if (!Q || !O || !staging || !state || !store->k_codes || !store->v_codes || !store->k_scales ||
+      !store->v_scales)
+    return H3KV_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(O) || !aligned16(staging) || !aligned16(state)) return H3KV_ERR_INVALID_ARG;
+  const int64_t kvb = kv_block == 0 ? H3KV_DEFAULT_KV_BLOCK : kv_block;
+  if (staging_bytes < h3kv_staging_bytes(store->heads, static_cast<int32_t>(kvb))) return H3KV_ERR_INVALID_ARG;
+  DeviceInfo *d = nullptr;
+  st = device_info(&d);
+  if (st != H3KV_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // staging layout: k codes [H, kvb, 128], v codes, k scales [H, kvb], v scales
+  int8_t *skc = static_cast<int8_t *>(staging);
+  int8_t *svc = skc + H * kvb * 128;
+  uint16_t *sks = reinterpret_cast<uint16_t *>(svc + H * kvb * 128);
+  uint16_t *svs = sks + H * kvb;
+  h3kv::AttnArgs a{};
+  a.q = Q;
+  a.k_codes = skc;
+  a.v_codes = svc;
+  a.k_scales = sks;
+  a.v_scales = svs;
+  a.o = O;
+  a.q_seq = q_seq;
+  a.kv_stride = kvb;
+  a.heads = store->heads;
+  a.scale_log2 = scale_log2_of(softmax_scale);
+  a.err = d->err;
+  a.timeout_ns = g_timeout_ns.load();
+  a.state = reinterpret_cast<float2 *>(state);
+  const int64_t n_blocks = (store->seq + kvb - 1) / kvb;
+  for (int64_t b = 0; b < n_blocks; ++b) {
+    const int64_t b0 = b * kvb;
+    const int64_t len = store->seq - b0 < kvb ? store->seq - b0 : kvb;
+    // one block of every head into the staging buffer (stream-ordered after
+    // the previous block's launches, which read the same buffer)
+    if (cudaMemcpy2DAsync(skc, kvb * 128, store->k_codes + b0 * 128, store->seq * 128, len * 128, H,
+                          cudaMemcpyDefault, s) != cudaSuccess ||
+        cudaMemcpy2DAsync(svc, kvb * 128, store->v_codes + b0 * 128, store->seq * 128, len * 128, H,
+                          cudaMemcpyDefault, s) != cudaSuccess ||
+        cudaMemcpy2DAsync(sks, kvb * 2, store->k_scales + b0, store->seq * 2, len * 2, H, cudaMemcpyDefault,
+                          s) != cudaSuccess ||
+        cudaMemcpy2DAsync(svs, kvb * 2, store->v_scales + b0, store->seq * 2, len * 2, H, cudaMemcpyDefault,
+                          s) != cudaSuccess)
+      return H3KV_ERR_CUDA;
+    a.kv_seq = len;
+    a.kv_block_tiles = static_cast<int32_t>((len + H3KV_KV_TILE - 1) / H3KV_KV_TILE);
+    a.stage_flags = (b == 0 ? 1 : 0) | (b == n_blocks - 1 ? 2 : 0);
+    for (int64_t c0 = 0; c0 < q_seq; c0 += q_chunk) {
+      a.q_begin = c0;
+      a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
+      if (h3kv::launch_attend_kvi8r(a, s) != cudaSuccess) return H3KV_ERR_CUDA;
+    }
   }
   return H3KV_OK;
 }

@@ -142,6 +142,20 @@ __device__ __forceinline__ void dequant_tile(uint8_t *tile, const uint16_t (&sc)
   }
 }
 
+// Log-sum-exp merge of a finished block (m_b, l_b) into the running (M, Lam)
+// (max in raw score units, c2 = softmax scale * log2 e): returns the weights
+// of the running and the block output and updates (M, Lam).  Written with
+// explicit fused operations so every merge -- inside one launch or across the
+// launches of the staged path -- rounds identically.
+__device__ __forceinline__ void lse_merge(float &M, float &Lam, float m_b, float l_b, float c2, float &al,
+                                          float &be) {
+  const float Mn = fmaxf(M, m_b);
+  al = ex2(__fmul_rn(__fsub_rn(M, Mn), c2));
+  be = ex2(__fmul_rn(__fsub_rn(m_b, Mn), c2));
+  Lam = __fmaf_rn(Lam, al, __fmul_rn(l_b, be));
+  M = Mn;
+}
+
 template <bool kKvi8r>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   if constexpr (kKvi8r) return pack_f16x2(lo, hi);
@@ -269,11 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool first = (j / blk) == 1;
           float al = 0.f, be = 1.f;
           if (!first) {
-            const float Mn = fmaxf(M, m_b);
-            al = ex2((M - Mn) * c2);
-            be = ex2((m_b - Mn) * c2);
-            Lam = Lam * al + l_b * be;
-            M = Mn;
+            lse_merge(M, Lam, m_b, l_b, c2, al, be);
           } else {
             M = m_b;
             Lam = l_b;
@@ -354,17 +364,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       // granule gi of row i at position gi ^ (i mod 32).  The K/V rings are
       // free now: every MMA has completed and no copy is outstanding.
       tc_fence_after();
-      uint8_t *stage = sm.k[0] + q * (kNQ * kTileBytes);
       const int n_blocks = (n_tiles + blk - 1) / blk;
+      // staged attention: this launch is one block of a sequence of launches
+      const bool staged = a.state != nullptr;
+      const bool first_launch = !staged || (a.stage_flags & 1);
+      const bool last_launch = !staged || (a.stage_flags & 2);
+      float2 *st = staged ? a.state + (static_cast<int64_t>(h) * a.q_seq + (row_ok ? row : 0)) : nullptr;
+      if (staged && !first_launch) {
+        // blocks of earlier launches: (M, Lam) from the state, their
+        // un-normalised output in the O row (n_blocks == 1 per staged launch)
+        const float2 m_l = row_ok ? *st : make_float2(0.f, 1.f);
+        M = m_l.x;
+        Lam = m_l.y;
+      }
+      const bool has_prev = n_blocks > 1 || !first_launch;
+      if (!last_launch) {
+        // not the last block: merge into the running output and state only
+        float al = 0.f, be = 1.f;
+        if (has_prev) {
+          lse_merge(M, Lam, m_b, l_b, c2, al, be);
+        } else {
+          M = m_b;
+          Lam = l_b;
+        }
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          float o[16];
+          tmem_ld16(tO + c * 16, *reinterpret_cast<uint32_t(*)[16]>(o));
+          if (row_ok) {
+            float4 *dst = reinterpret_cast<float4 *>(orow + c * 16);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              float4 v = make_float4(o[4 * k] * be, o[4 * k + 1] * be, o[4 * k + 2] * be, o[4 * k + 3] * be);
+              if (has_prev) {
+                const float4 g = dst[k];
+                v.x = fmaf(g.x, al, v.x);
+                v.y = fmaf(g.y, al, v.y);
+                v.z = fmaf(g.z, al, v.z);
+                v.w = fmaf(g.w, al, v.w);
+              }
+              dst[k] = v;
+            }
+          }
+        }
+        if (row_ok) *st = make_float2(M, Lam);
+      } else {
+      uint8_t *stage = sm.k[0] + q * (kNQ * kTileBytes);
       float ga, gb;
-      if (n_blocks == 1) {
+      if (!has_prev) {
         ga = 0.f;
         gb = 1.f / l_b;
       } else {
-        const float Mn = fmaxf(M, m_b);
-        const float al = ex2((M - Mn) * c2);
-        const float be = ex2((m_b - Mn) * c2);
-        const float inv = 1.f / (Lam * al + l_b * be);
+        float al, be;
+        lse_merge(M, Lam, m_b, l_b, c2, al, be);
+        const float inv = 1.f / Lam;
         ga = al * inv;
         gb = be * inv;
       }
@@ -374,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tO + c * 32, *reinterpret_cast<uint32_t(*)[32]>(o));
 #pragma unroll
         for (int k = 0; k < 32; ++k) o[k] *= gb;
-        if (n_blocks > 1 && row_ok) {
+        if (has_prev && row_ok) {
           const float4 *src = reinterpret_cast<const float4 *>(orow + c * 32);
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
@@ -411,14 +464,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<float4 *>(a.o + (static_cast<int64_t>(h) * a.q_seq + r) * 128 + 4 * lane) =
               make_float4(x[0], x[1], x[2], x[3]);
       }
+      }
     }
   } else if (warp < 12) {
     // ======================================================= dequantisers
     reg_dealloc<kKvi8r ? kRegDequantKvi8r : kRegDequantExact>();
     if constexpr (kKvi8r) {
       const int dw = warp - 8;
-      const uint16_t *ksc = a.k_scales + static_cast<int64_t>(h) * a.kv_seq;
-      const uint16_t *vsc = a.v_scales + static_cast<int64_t>(h) * a.kv_seq;
+      const uint16_t *ksc = a.k_scales + static_cast<int64_t>(h) * a.kv_stride;
+      const uint16_t *vsc = a.v_scales + static_cast<int64_t>(h) * a.kv_stride;
       uint16_t sck[8], scv[8];
       for (int j = 0; j < n_tiles; ++j) {
         const int64_t tok0 = static_cast<int64_t>(j) * kBN;
@@ -465,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (kKvi8r) {
             const uint32_t bytes = static_cast<uint32_t>((a.kv_seq - tok0 < kBN ? a.kv_seq - tok0 : kBN) * 128);
             mbar_arrive_expect_tx(bar, bytes);
-            bulk_g2s(smem_u32(sm.k[ks] + kChunkBytes), a.k_codes + (static_cast<int64_t>(h) * a.kv_seq + tok0) * 128,
+            bulk_g2s(smem_u32(sm.k[ks] + kChunkBytes), a.k_codes + (static_cast<int64_t>(h) * a.kv_stride + tok0) * 128,
                      bytes, bar);
           } else {
             mbar_arrive_expect_tx(bar, kTileBytes);
@@ -480,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (kKvi8r) {
             const uint32_t bytes = static_cast<uint32_t>((a.kv_seq - tok0 < kBN ? a.kv_seq - tok0 : kBN) * 128);
             mbar_arrive_expect_tx(bar, bytes);
-            bulk_g2s(smem_u32(sm.v[vs] + kChunkBytes), a.v_codes + (static_cast<int64_t>(h) * a.kv_seq + tok0) * 128,
+            bulk_g2s(smem_u32(sm.v[vs] + kChunkBytes), a.v_codes + (static_cast<int64_t>(h) * a.kv_stride + tok0) * 128,
                      bytes, bar);
           } else {
             mbar_arrive_expect_tx(bar, kTileBytes);

@@ -26,7 +26,8 @@ struct AttnArgs {
   const uint16_t *v_scales;
   float *o;                 // fp32 [heads, q_seq, 128]
   int64_t q_seq;
-  int64_t kv_seq;
+  int64_t kv_seq;           // keys attended by this launch
+  int64_t kv_stride;        // rows between heads in the K/V store arrays (kv_seq unless staged)
   int64_t q_begin;          // this launch's query chunk [q_begin, q_end)
   int64_t q_end;
   int32_t heads;
@@ -34,6 +35,12 @@ struct AttnArgs {
   float scale_log2;         // softmax_scale * log2(e)
   uint32_t *err;
   uint64_t timeout_ns;
+  // Staged attention (one kv_block per launch, blocks in order): running
+  // (max, sum) per query row [heads, q_seq], carried between launches with O
+  // as the running un-normalised output; nullptr for a single launch over all
+  // keys.  stage_flags: bit 0 = first block, bit 1 = last block.
+  float2 *state;
+  int32_t stage_flags;
 };
 
 constexpr int kAttnRowsPerCta = 256;  // two 128-row query tiles per CTA

@@ -92,3 +92,26 @@ def test_binding_raises_on_error_status():
 def test_wait_timeout_setter_needs_no_device():
     assert b.h3kv_set_wait_timeout_ns(5000) == b.H3KV_OK
     assert b.h3kv_set_wait_timeout_ns(0) == b.H3KV_OK
+
+
+def test_staging_bytes():
+    assert b.h3kv_staging_bytes(32, 16384) == 2 * 32 * 16384 * 130
+    assert b.h3kv_staging_bytes(2, 0) == 2 * 2 * 16384 * 130
+    assert b.h3kv_staging_bytes(2, 100) == 0
+    assert b.h3kv_staging_bytes(-1, 128) == 0
+
+
+def test_attend_staged_rejects_bad_arguments():
+    st = _store()
+    at = b.h3kv_attend_staged
+    big = b.h3kv_staging_bytes(1, 256)
+    assert at(4096, 256, None, 256, 256, 0.0, 4096, 4096, big, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    assert at(4096, 256, ctypes.byref(st), 0, 256, 0.0, 4096, 4096, big, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    assert at(4096, 256, ctypes.byref(st), 64, 200, 0.0, 4096, 4096, big, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    assert at(4096, 256, ctypes.byref(st), 64, 256, 0.0, 4096, 0, big, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    assert at(4096, 256, ctypes.byref(st), 64, 256, 0.0, 4096, 4096, big, 0, None) == b.H3KV_ERR_INVALID_ARG
+    assert at(4096, 256, ctypes.byref(st), 64, 256, 0.0, 4096, 4096, big - 1, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    assert at(4096, 256, ctypes.byref(st), 64, 256, 0.0, 4096, 4104, big, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    assert at(4096, 256, ctypes.byref(_store(head_dim=64)), 64, 256, 0.0, 4096, 4096, big, 4096,
+              None) == b.H3KV_ERR_UNSUPPORTED
+    assert at(4096, 0, ctypes.byref(st), 64, 256, 0.0, 4096, 4096, big, 4096, None) == b.H3KV_OK

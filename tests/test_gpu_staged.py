@@ -1,0 +1,62 @@
+"""kvi8r attention over a store held outside HBM, staged one kv_block at a time.
+
+The kv_block row of the H3 Streamed Blocks Inputs table keeps the blockwise
+log-sum-exp combine "for the host-staged K/V design to come".
+h3kv_attend_staged copies each block of the store (here in pinned Grace
+memory) into an HBM staging buffer, attends every query chunk over it, and
+carries the combine across blocks in a per-row (max, sum) state.  Its output
+must be bit-identical to h3kv_attend over the same store with the same
+q_chunk and kv_block, and match the oracle.
+"""
+import pytest
+import torch
+
+import oracle
+from parity import compare_attention
+from store_h3kv_build_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _b():
+    from store_h3kv_build_gb300 import binding as b
+    return b
+
+
+@pytest.mark.parametrize("heads,q_seq,kv_seq,q_chunk,kv_block", [
+    (1, 1024, 1024, 256, 512),      # two blocks
+    (2, 1000, 1337, 300, 256),      # six blocks, ragged last block and query chunks
+    (3, 129, 5, 64, 128),           # one block shorter than a tile
+    (1, 4096, 4096, 4096, 0),       # kv_block 16384 > sequence: one block
+    (2, 700, 3000, 256, 1024),      # three blocks, last one ragged
+])
+def test_staged_bit_identical_to_resident(cuda, heads, q_seq, kv_seq, q_chunk, kv_block):
+    b = _b()
+    q, k, v = synth.make_qkv(heads, kv_seq, seed=31, q_seq=q_seq, k_outliers=True)
+    qd = q.to(cuda)
+    dev = b.build_store(k.to(cuda), v.to(cuda))
+    host = b.build_store(k.to(cuda), v.to(cuda), out=b.Store.empty(heads, kv_seq, host=True))
+    ref = b.attend(qd, dev, q_chunk=q_chunk, kv_block=kv_block)
+    staged_host = b.attend_staged(qd, host, q_chunk=q_chunk, kv_block=kv_block)
+    staged_dev = b.attend_staged(qd, dev, q_chunk=q_chunk, kv_block=kv_block)
+    b.sync_status()
+    assert torch.equal(staged_host, ref)
+    assert torch.equal(staged_dev, ref)
+    compare_attention(staged_host, oracle.attend(q, oracle.build_store(k, v)), f"staged {heads}x{q_seq}x{kv_seq}")
+
+
+def test_staged_reuses_scratch_across_calls(cuda):
+    # the same staging buffer and state serve consecutive calls; nothing of a
+    # previous call may leak into the next
+    b = _b()
+    heads, seq, kvb = 2, 2000, 512
+    staging = torch.empty(b.h3kv_staging_bytes(heads, kvb), dtype=torch.uint8, device=cuda)
+    state = torch.full((heads, seq, 2), float("nan"), dtype=torch.float32, device=cuda)
+    outs = []
+    for seed in (41, 42, 41):
+        q, k, v = synth.make_qkv(heads, seq, seed=seed)
+        host = b.build_store(k.to(cuda), v.to(cuda), out=b.Store.empty(heads, seq, host=True))
+        outs.append(b.attend_staged(q.to(cuda), host, q_chunk=700, kv_block=kvb, staging=staging, state=state))
+    b.sync_status()
+    assert torch.equal(outs[0], outs[2])
+    assert not torch.equal(outs[0], outs[1])
