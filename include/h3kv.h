@@ -135,6 +135,30 @@ h3kv_status h3kv_attend_staged(const uint16_t *Q, int64_t q_seq, const h3kv_stor
                                int32_t kv_block, float softmax_scale, float *O, void *staging,
                                size_t staging_bytes, float *state, void *stream);
 
+/* Size of the fixed device scratch that h3kv_attend_staged_static uses. */
+#define H3KV_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* h3kv_attend_staged with no caller-provided scratch (no counterpart on the
+ * kvi8r pages; it exists for callers that cannot allocate device memory -- a
+ * plugin whose host application owns the whole device-memory budget, or code
+ * on a path where a cudaMalloc, which can synchronise the device, is not
+ * allowed).  The staging block and the per-row state live in a fixed
+ * H3KV_STATIC_SCRATCH_BYTES array that the library holds on every GPU that
+ * loads it, until the process exits.  The caller still passes Q, the store
+ * and O; the library allocates nothing.
+ *   Limit: round_up(h3kv_staging_bytes(store->heads, kv_block), 256)
+ *          + store->heads * q_seq * 8  <=  H3KV_STATIC_SCRATCH_BYTES,
+ *   otherwise H3KV_ERR_INVALID_ARG is returned before any device work.
+ *   The first call on a device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   Every call shares the array and leaves its contents behind; nothing in
+ *   it needs to start at zero.  Calls that overlap on the GPU (other streams,
+ *   other threads) race on it: run them one after another.
+ * Results equal h3kv_attend_staged's. */
+h3kv_status h3kv_attend_staged_static(const uint16_t *Q, int64_t q_seq, const h3kv_store *store,
+                                      int32_t q_chunk, int32_t kv_block, float softmax_scale, float *O,
+                                      void *stream);
+
 /* Synchronise `stream`, then return and clear the device error word that the
  * kernels set when a bounded wait runs out (H3KV_ERR_DEVICE_TIMEOUT), or
  * H3KV_ERR_CUDA if the synchronisation itself reports an error. */

@@ -50,6 +50,8 @@ _SIGS = {
     "h3kv_attend_exact": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _f32, _vp, _vp]),
     "h3kv_sync_status": (ctypes.c_int, [_vp]),
     "h3kv_staging_bytes": (ctypes.c_size_t, [_i32, _i32]),
+    "h3kv_attend_staged_static": (ctypes.c_int, [_vp, _i64, ctypes.POINTER(h3kv_store), _i32, _i32, _f32, _vp,
+                                                 _vp]),
     "h3kv_attend_staged": (ctypes.c_int, [_vp, _i64, ctypes.POINTER(h3kv_store), _i32, _i32, _f32, _vp, _vp,
                                           ctypes.c_size_t, _vp, _vp]),
     "h3kv_set_wait_timeout_ns": (ctypes.c_int, [ctypes.c_uint64]),
