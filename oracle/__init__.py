@@ -7,5 +7,5 @@ path and imports nothing from it.
 from .kvi8r import (  # noqa: F401
     HEAD_DIM, as_f64, hadamard, rotate, unrotate, fp16_round, row_scales, quantize,
     encode_rows, build_store, dequant, default_scale, softmax_attention, attend,
-    attend_exact, attend_blockwise, rel_rms,
+    attend_exact, attend_blockwise, rel_rms, group_scales, encode_rows_grouped, build_store_grouped,
 )

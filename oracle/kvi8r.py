@@ -41,6 +41,11 @@ the pages supports):
       smallest fp16 subnormal) has all codes 0.
   R6  softmax scale defaults to 1/sqrt(128); attention is non-causal and
       unmasked; output is fp32 (this oracle returns fp64).
+  R8  the per-32-value variant (the write-up's roadmap: "a per-32-value
+      scale variant of kvi8r (finer than per row)") splits each rotated row
+      into 4 consecutive groups of 32 values and gives each group its own
+      scale, defined as in R2-R5 over the group; dequantisation multiplies
+      each code by its group's scale.
   R7  kv_block does not change the mathematical result: the blockwise
       log-sum-exp combine equals one full softmax.  ``attend`` uses one full
       softmax; ``attend_blockwise`` follows the blockwise description and is
@@ -141,8 +146,39 @@ def build_store(K, V) -> dict:
 
 def dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     """K^' = code * scale (the pages' int8->fp16 cast times the scale, here in
-    exact fp64)."""
-    return codes.astype(np.float64) * np.asarray(scales, np.float64)[..., None]
+    exact fp64).  Per-row scales have one axis fewer than the codes; per-group
+    scales (reading R8) have a last axis of 128/group, each covering that many
+    consecutive values."""
+    scales = np.asarray(scales, np.float64)
+    if scales.ndim == codes.ndim:  # per-group scales
+        group = codes.shape[-1] // scales.shape[-1]
+        return codes.astype(np.float64) * np.repeat(scales, group, axis=-1)
+    return codes.astype(np.float64) * scales[..., None]
+
+
+# --------------------------------------------------------------------------
+# per-32-value scale variant (reading R8)
+# --------------------------------------------------------------------------
+def group_scales(xr: np.ndarray, group: int = 32) -> np.ndarray:
+    """One fp16 scale per `group` consecutive rotated values (R2, R3 per
+    group): shape [..., 128/group]."""
+    g = xr.reshape(*xr.shape[:-1], xr.shape[-1] // group, group)
+    return row_scales(g)
+
+
+def encode_rows_grouped(x, group: int = 32) -> tuple[np.ndarray, np.ndarray]:
+    """Rotate, then quantise every group of `group` values with its own scale."""
+    xr = rotate(x)
+    s = group_scales(xr, group)
+    g = xr.reshape(*xr.shape[:-1], xr.shape[-1] // group, group)
+    codes = quantize(g, s).reshape(xr.shape)
+    return codes, s
+
+
+def build_store_grouped(K, V, group: int = 32) -> dict:
+    kc, ks = encode_rows_grouped(K, group)
+    vc, vs = encode_rows_grouped(V, group)
+    return {"k_codes": kc, "k_scales": ks, "v_codes": vc, "v_scales": vs}
 
 
 # --------------------------------------------------------------------------

@@ -303,3 +303,64 @@ def test_attend_heads_subset_matches_full():
     full = oracle.attend(Q, st)
     part = oracle.attend(oracle.as_f64(Q)[[2, 0]], st, heads=[2, 0])
     assert np.array_equal(part, full[[2, 0]])
+
+
+# ------------------------------------------------ per-32-value scales (R8) --
+def test_grouped_scales_hand_example():
+    # A rotated row whose 4 groups of 32 have maxima 127, 12.7, 1.27 and 0:
+    # scales are fp16(1), fp16(0.1), fp16(0.01) and 0, and each group's
+    # absmax entry quantises to +-127 with its own scale.
+    xr = np.zeros((1, 128))
+    xr[0, 5], xr[0, 40], xr[0, 70] = 127.0, -12.7, 1.27
+    xr[0, 6] = 0.5
+    s = oracle.group_scales(xr)
+    assert s.shape == (1, 4)
+    expect = torch.tensor([1.0, 0.1, 0.01], dtype=torch.float64).to(torch.float16).double().numpy()
+    assert np.array_equal(s[0, :3], expect) and s[0, 3] == 0
+    g = xr.reshape(1, 4, 32)
+    codes = oracle.quantize(g, s).reshape(1, 128)
+    assert codes[0, 5] == 127 and codes[0, 40] == -127 and codes[0, 70] == 127
+    assert codes[0, 6] == 0  # 0.5 / fp16(1) = 0.5 -> ties to even -> 0
+    assert not codes[0, 96:].any()
+
+
+def test_grouped_roundtrip_bound_and_reach():
+    x = oracle.as_f64(bf16_normal((3, 200, 128), 71))
+    x[0, :, 17] *= 20
+    codes, s = oracle.encode_rows_grouped(x)
+    xr = oracle.rotate(x)
+    assert s.shape == (3, 200, 4)
+    err = np.abs(oracle.dequant(codes, s) - xr)
+    assert np.all(err <= np.repeat(s, 32, axis=-1) / 2 * (1 + 1e-12))
+    assert np.all(np.abs(codes.reshape(3, 200, 4, 32)).max(axis=-1) == 127)
+
+
+def test_group_of_128_is_the_per_row_store():
+    x = oracle.as_f64(bf16_normal((2, 50, 128), 72))
+    c1, s1 = oracle.encode_rows(x)
+    c2, s2 = oracle.encode_rows_grouped(x, group=128)
+    assert np.array_equal(c1, c2) and np.array_equal(s1, s2[..., 0])
+
+
+def test_grouped_scales_are_never_coarser():
+    # each group's scale is at most the row's scale, so the error never grows
+    x = oracle.as_f64(bf16_normal((1, 500, 128), 73))
+    x[0, :, [3, 77]] *= 20
+    _, s_row = oracle.encode_rows(x)
+    cg, s_grp = oracle.encode_rows_grouped(x)
+    assert np.all(s_grp <= s_row[..., None])
+    cr, _ = oracle.encode_rows(x)
+    xr = oracle.rotate(x)
+    e_row = np.abs(oracle.dequant(cr, s_row) - xr).mean()
+    e_grp = np.abs(oracle.dequant(cg, s_grp) - xr).mean()
+    assert e_grp < e_row
+
+
+def test_grouped_attention_closer_to_exact():
+    Q = bf16_normal((2, 64, 128), 74)
+    K = bf16_normal((2, 512, 128), 75)
+    V = bf16_normal((2, 512, 128), 76)
+    ex = oracle.attend_exact(Q, K, V)
+    r_row = oracle.rel_rms(oracle.attend(Q, oracle.build_store(K, V)), ex)
+    r_grp = oracle.rel_rms(oracle.attend(Q, oracle.build_store_grouped(K, V)), ex)
+    assert r_grp < r_row
