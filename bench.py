@@ -283,6 +283,23 @@ def run_ours(args, w, name):
     b.sync_status()
     exact_ms = xs.elapsed_time(xe) / n_exact
 
+    # ---- the per-32-value scale variant (the write-up's roadmap) on the same
+    # inputs: store build and attention
+    gst = b.Store.empty(H, L, dev, scale_group=32)
+    b.build_store(k, v, out=gst)
+    b.attend(q, gst, q_chunk=q_chunk, kv_block=kv_block, out=out)
+    gs, gm, ge = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    gs.record(stream)
+    b.build_store(k, v, out=gst)
+    gm.record(stream)
+    b.attend(q, gst, q_chunk=q_chunk, kv_block=kv_block, out=out)
+    ge.record(stream)
+    torch.cuda.synchronize(dev)
+    b.sync_status()
+    g32_build_ms, g32_attend_ms = gs.elapsed_time(gm), gm.elapsed_time(ge)
+    g32_bytes = store_bytes(H, L) + 2 * H * L * 6
+    del gst
+
     # ---- the same store held in pinned Grace memory and staged into HBM one
     # kv_block at a time (the pages keep kv_block for a host-staged K/V design)
     hst = b.Store.empty(H, L, host=True)
@@ -354,6 +371,9 @@ def run_ours(args, w, name):
             "attend_ms": attend_sum / args.steps,
             "exact_attend": {"ms": exact_ms, "tflops": flops / (exact_ms / 1e3) / 1e12,
                              "kvi8r_over_exact_time": (attend_sum / args.steps) / exact_ms},
+            "g32_store": {"what": "one fp16 scale per 32 rotated values",
+                          "attend_ms": g32_attend_ms, "attend_tflops": flops / (g32_attend_ms / 1e3) / 1e12,
+                          "build_ms": g32_build_ms, "build_gbs": g32_bytes / (g32_build_ms / 1e3) / 1e9},
             "host_store": {"where": "kvi8r store built into pinned Grace memory over NVLink-C2C, attended "
                                     "with h3kv_attend_staged (each kv_block copied into HBM, copies timed)",
                            "attend_ms": host_attend_ms, "attend_tflops": flops / (host_attend_ms / 1e3) / 1e12,

@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define H3KV_ABI_VERSION 1u
+#define H3KV_ABI_VERSION 2u
 #define H3KV_HEAD_DIM 128
 /* kv_block = 0 on the kvi8r path means this many tokens (the kv_block
  * default of the kv_store row). */
@@ -52,13 +52,20 @@ typedef enum {
   H3KV_ERR_DEVICE_TIMEOUT = 4  /* a bounded in-kernel wait ran out           */
 } h3kv_status;
 
-/* The kvi8r store: for K and for V, int8 codes [heads, seq, 128] and one fp16
- * scale per (head, token) row [heads, seq].  The codes are the rows of K (or
- * V) rotated into the orthonormal Sylvester-Hadamard basis H (x' = x H, H the
- * order-128 Hadamard matrix / sqrt(128)), quantised as
- *   s = fp16_rne(max_j |x'_j| / 127)   (saturated at 65504),
+/* The kvi8r store: for K and for V, int8 codes [heads, seq, 128] and fp16
+ * scales.  The codes are the rows of K (or V) rotated into the orthonormal
+ * Sylvester-Hadamard basis H (x' = x H, H the order-128 Hadamard matrix /
+ * sqrt(128)), quantised per scale group G of consecutive rotated values as
+ *   s = fp16_rne(max_{j in G} |x'_j| / 127)   (saturated at 65504),
  *   c_j = clamp(rne(x'_j / s), -127, 127),   c = 0 where s == 0.
- * Dequantisation is c * s.  All four buffers are caller-owned device memory. */
+ * Dequantisation is c * s.  scale_group selects the group:
+ *   0 or 128: one scale per (head, token) row (the kv_store row of the H3
+ *             Streamed Blocks Inputs table); scales are [heads, seq];
+ *   32:       one scale per 32 values (the "per-32-value scale variant of
+ *             kvi8r" of the Low VRAM write-up's roadmap); scales are
+ *             [heads, seq, 4].
+ * All four buffers are caller-owned memory (device memory, or host memory
+ * the GPU can address -- see h3kv_attend_staged). */
 typedef struct {
   int8_t *k_codes;
   int8_t *v_codes;
@@ -66,14 +73,16 @@ typedef struct {
   uint16_t *v_scales; /* fp16 bit patterns */
   int32_t heads;
   int64_t seq;
-  int32_t head_dim; /* must be 128 */
+  int32_t head_dim;    /* must be 128 */
+  int32_t scale_group; /* 0 or 128 (per row) or 32 */
 } h3kv_store;
 
 /* Version of this ABI (H3KV_ABI_VERSION). */
 uint32_t h3kv_abi_version(void);
 
-/* Bytes of device memory a store of this shape occupies in total (codes and
- * scales of K and V): 2 * heads * seq * (head_dim + 2).  Returns 0 for
+/* Bytes of device memory a per-row-scale store of this shape occupies in
+ * total (codes and scales of K and V): 2 * heads * seq * (head_dim + 2); a
+ * scale_group 32 store holds 6 more bytes per row and tensor.  Returns 0 for
  * invalid shapes. */
 size_t h3kv_store_bytes(int32_t heads, int64_t seq, int32_t head_dim);
 
@@ -128,7 +137,9 @@ size_t h3kv_staging_bytes(int32_t heads, int32_t kv_block);
  * query row) with O itself as the running un-normalised output.  The result
  * is bit-identical to h3kv_attend on the same store, q_chunk and kv_block.
  * Arguments otherwise as h3kv_attend; `store` may point to host (pinned for
- * asynchronous copies) or device memory.  The library allocates nothing:
+ * asynchronous copies) or device memory, and must have per-row scales
+ * (scale_group 0 or 128; H3KV_ERR_UNSUPPORTED otherwise).  The library
+ * allocates nothing:
  * staging and state are caller-owned scratch, reused by each call, so calls
  * that overlap on the GPU must not share them. */
 h3kv_status h3kv_attend_staged(const uint16_t *Q, int64_t q_seq, const h3kv_store *store, int32_t q_chunk,

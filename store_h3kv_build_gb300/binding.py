@@ -38,6 +38,7 @@ class h3kv_store(ctypes.Structure):  # noqa: N801 - mirrors the C struct name
         ("heads", ctypes.c_int32),
         ("seq", ctypes.c_int64),
         ("head_dim", ctypes.c_int32),
+        ("scale_group", ctypes.c_int32),
     ]
 
 
@@ -95,9 +96,11 @@ class Store:
         self.k_codes, self.v_codes = k_codes, v_codes
         self.k_scales, self.v_scales = k_scales, v_scales
         self.heads, self.seq = int(k_codes.shape[0]), int(k_codes.shape[1])
+        # [heads, seq] scales: one per row; [heads, seq, 4]: one per 32 values
+        self.scale_group = 32 if k_scales.dim() == 3 else 0
 
     @classmethod
-    def empty(cls, heads: int, seq: int, device="cuda", host: bool = False) -> "Store":
+    def empty(cls, heads: int, seq: int, device="cuda", host: bool = False, scale_group: int = 0) -> "Store":
         """Uninitialised store buffers.  ``host=True`` places them in pinned
         host memory: on a Grace-Blackwell node the kernels read (and the
         store build writes) them directly over NVLink-C2C, so the whole
@@ -108,7 +111,8 @@ class Store:
             kw = dict(device=device)
         kc = torch.empty((heads, seq, HEAD_DIM), dtype=torch.int8, **kw)
         vc = torch.empty_like(kc)
-        ks = torch.empty((heads, seq), dtype=torch.float16, **kw)
+        sshape = (heads, seq, HEAD_DIM // 32) if scale_group == 32 else (heads, seq)
+        ks = torch.empty(sshape, dtype=torch.float16, **kw)
         vs = torch.empty_like(ks)
         return cls(kc, vc, ks, vs)
 
@@ -118,16 +122,18 @@ class Store:
 
     def c_struct(self) -> h3kv_store:
         return h3kv_store(_ptr(self.k_codes), _ptr(self.v_codes), _ptr(self.k_scales), _ptr(self.v_scales),
-                          self.heads, self.seq, HEAD_DIM)
+                          self.heads, self.seq, HEAD_DIM, self.scale_group)
 
     def nbytes(self) -> int:
         return int(h3kv_store_bytes(self.heads, self.seq, HEAD_DIM))
 
 
-def build_store(K: torch.Tensor, V: torch.Tensor, out: Store | None = None, stream=None) -> Store:
-    """h3kv_build_store on bf16 K, V [heads, seq, 128] (CUDA, contiguous)."""
+def build_store(K: torch.Tensor, V: torch.Tensor, out: Store | None = None, stream=None,
+                scale_group: int = 0) -> Store:
+    """h3kv_build_store on bf16 K, V [heads, seq, 128] (CUDA, contiguous);
+    scale_group 32 gives one scale per 32 rotated values."""
     heads, seq = int(K.shape[0]), int(K.shape[1])
-    out = Store.empty(heads, seq, K.device) if out is None else out
+    out = Store.empty(heads, seq, K.device, scale_group=scale_group) if out is None else out
     st = out.c_struct()
     check(h3kv_build_store(_ptr(K), _ptr(V), heads, seq, int(K.shape[2]), ctypes.byref(st), _stream(stream)),
           "h3kv_build_store")

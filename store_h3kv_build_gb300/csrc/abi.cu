@@ -117,6 +117,14 @@ h3kv_status check_chunks(int32_t q_chunk, int32_t kv_block) {
   return H3KV_OK;
 }
 
+// Scales per row of a store: 1 (scale_group 0 or 128) or 4 (scale_group 32);
+// 0 for an invalid scale_group.
+int scale_groups_of(const h3kv_store *st) {
+  if (st->scale_group == 0 || st->scale_group == 128) return 1;
+  if (st->scale_group == 32) return 4;
+  return 0;
+}
+
 float scale_log2_of(float softmax_scale) {
   const float s = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(128.0f);
   return s * 1.4426950408889634f;
@@ -150,6 +158,8 @@ h3kv_status h3kv_build_store(const uint16_t *K, const uint16_t *V, int32_t heads
   if (heads < 0 || seq < 0 || !out) return H3KV_ERR_INVALID_ARG;
   if (head_dim != H3KV_HEAD_DIM || out->head_dim != H3KV_HEAD_DIM) return H3KV_ERR_UNSUPPORTED;
   if (out->heads != heads || out->seq != seq) return H3KV_ERR_INVALID_ARG;
+  const int groups = scale_groups_of(out);
+  if (groups == 0) return H3KV_ERR_INVALID_ARG;
   const int64_t rows = static_cast<int64_t>(heads) * seq;
   if (rows == 0) return H3KV_OK;
   if (rows > kMaxRows) return H3KV_ERR_INVALID_ARG;
@@ -167,7 +177,7 @@ h3kv_status h3kv_build_store(const uint16_t *K, const uint16_t *V, int32_t heads
       !encode_2d(&v_out, CU_TENSOR_MAP_DATA_TYPE_UINT8, out->v_codes, rows, 1, 128))
     return H3KV_ERR_CUDA;
   const cudaError_t e = h3kv::launch_store_build(k_in, v_in, k_out, v_out, out->k_scales, out->v_scales, rows,
-                                                 d->num_sms, d->err, g_timeout_ns.load(),
+                                                 d->num_sms, groups, d->err, g_timeout_ns.load(),
                                                  static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? H3KV_OK : H3KV_ERR_CUDA;
 }
@@ -178,6 +188,8 @@ h3kv_status h3kv_attend(const uint16_t *Q, int64_t q_seq, const h3kv_store *stor
   if (store->head_dim != H3KV_HEAD_DIM) return H3KV_ERR_UNSUPPORTED;
   h3kv_status st = check_chunks(q_chunk, kv_block);
   if (st != H3KV_OK) return st;
+  const int groups = scale_groups_of(store);
+  if (groups == 0) return H3KV_ERR_INVALID_ARG;
   if (store->heads == 0 || q_seq == 0) return H3KV_OK;
   if (store->seq == 0) return H3KV_ERR_INVALID_ARG;
   if (static_cast<int64_t>(store->heads) * q_seq > kMaxRows || static_cast<int64_t>(store->heads) * store->seq > kMaxRows)
@@ -201,6 +213,7 @@ h3kv_status h3kv_attend(const uint16_t *Q, int64_t q_seq, const h3kv_store *stor
   a.q_seq = q_seq;
   a.kv_seq = store->seq;
   a.kv_stride = store->seq;
+  a.scale_groups = groups;
   a.heads = store->heads;
   a.kv_block_tiles = kvb / H3KV_KV_TILE;
   a.scale_log2 = scale_log2_of(softmax_scale);
@@ -242,6 +255,7 @@ h3kv_status h3kv_attend_exact(const uint16_t *Q, int64_t q_seq, const uint16_t *
   a.q_seq = q_seq;
   a.kv_seq = kv_seq;
   a.kv_stride = kv_seq;
+  a.scale_groups = 1;
   a.heads = heads;
   a.kv_block_tiles = kv_block == 0 ? static_cast<int32_t>(n_tiles) : kv_block / H3KV_KV_TILE;
   a.scale_log2 = scale_log2_of(softmax_scale);
@@ -269,6 +283,8 @@ h3kv_status h3kv_attend_staged(const uint16_t *Q, int64_t q_seq, const h3kv_stor
   if (store->head_dim != H3KV_HEAD_DIM) return H3KV_ERR_UNSUPPORTED;
   h3kv_status st = check_chunks(q_chunk, kv_block);
   if (st != H3KV_OK) return st;
+  if (scale_groups_of(store) == 0) return H3KV_ERR_INVALID_ARG;
+  if (scale_groups_of(store) != 1) return H3KV_ERR_UNSUPPORTED;
   if (store->heads == 0 || q_seq == 0) return H3KV_OK;
   if (store->seq == 0) return H3KV_ERR_INVALID_ARG;
   const int64_t H = store->heads;
@@ -302,6 +318,7 @@ h3kv_status h3kv_attend_staged(const uint16_t *Q, int64_t q_seq, const h3kv_stor
   a.err = d->err;
   a.timeout_ns = g_timeout_ns.load();
   a.state = reinterpret_cast<float2 *>(state);
+  a.scale_groups = 1;
   const int64_t n_blocks = (store->seq + kvb - 1) / kvb;
   for (int64_t b = 0; b < n_blocks; ++b) {
     const int64_t b0 = b * kvb;

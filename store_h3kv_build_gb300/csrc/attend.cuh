@@ -108,13 +108,17 @@ __device__ __forceinline__ uint32_t dq_granule(int lane) {
   return (lane & 3) + 4 * (hf ^ (q4 & 1));
 }
 
-// Scales of the rows this lane dequantises (rows past `valid` get 0).
+// Scales of the rows this lane dequantises (rows past `valid` get 0).  With
+// kGroups = 4 a row has one scale per 32 values and the lane's 16-value
+// granule g takes scale g / 2 of its row.
+template <int kGroups>
 __device__ __forceinline__ void dequant_scales(const uint16_t *scales, int valid, int dw, int lane,
                                                uint16_t (&sc)[8]) {
+  const int grp = kGroups == 1 ? 0 : static_cast<int>(dq_granule(lane) >> 1);
 #pragma unroll
   for (int it = 0; it < 8; ++it) {
     const int r = static_cast<int>(dq_row(dw, it, lane));
-    sc[it] = r < valid ? scales[r] : 0;
+    sc[it] = r < valid ? scales[r * kGroups + grp] : 0;
   }
 }
 
@@ -162,7 +166,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   else return pack_bf16x2(lo, hi);
 }
 
-template <bool kKvi8r>
+template <bool kKvi8r, int kGroups>
 __global__ void __launch_bounds__(kThreads, 1)
     attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
@@ -471,16 +475,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     reg_dealloc<kKvi8r ? kRegDequantKvi8r : kRegDequantExact>();
     if constexpr (kKvi8r) {
       const int dw = warp - 8;
-      const uint16_t *ksc = a.k_scales + static_cast<int64_t>(h) * a.kv_stride;
-      const uint16_t *vsc = a.v_scales + static_cast<int64_t>(h) * a.kv_stride;
+      const uint16_t *ksc = a.k_scales + static_cast<int64_t>(h) * a.kv_stride * kGroups;
+      const uint16_t *vsc = a.v_scales + static_cast<int64_t>(h) * a.kv_stride * kGroups;
       uint16_t sck[8], scv[8];
       for (int j = 0; j < n_tiles; ++j) {
         const int64_t tok0 = static_cast<int64_t>(j) * kBN;
         const int valid = static_cast<int>(a.kv_seq - tok0 < kBN ? a.kv_seq - tok0 : kBN);
         const int ks = j % kNK, vs = j % kNV;
         // scale loads go out before the waits so their latency hides there
-        dequant_scales(ksc + tok0, valid, dw, lane, sck);
-        dequant_scales(vsc + tok0, valid, dw, lane, scv);
+        dequant_scales<kGroups>(ksc + tok0 * kGroups, valid, dw, lane, sck);
+        dequant_scales<kGroups>(vsc + tok0 * kGroups, valid, dw, lane, scv);
         if (!warp_wait(smem_u32(&sm.k_load[ks]), (j / kNK) & 1, wctx)) break;
         dequant_tile(sm.k[ks], sck, dw, lane);
         fence_proxy_async_smem();

@@ -7,12 +7,12 @@ cudaError_t launch_attend_exact(const CUtensorMap &q, const CUtensorMap &k, cons
                                 const AttnArgs &args, cudaStream_t stream) {
   const int64_t rows = args.q_end - args.q_begin;
   if (rows <= 0 || args.heads <= 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(attn::attend_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(attn::attend_kernel<false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(attn::kSmemBytes));
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>((rows + kAttnRowsPerCta - 1) / kAttnRowsPerCta),
                   static_cast<unsigned>(args.heads));
-  attn::attend_kernel<false><<<grid, attn::kThreads, attn::kSmemBytes, stream>>>(q, k, v, args);
+  attn::attend_kernel<false, 1><<<grid, attn::kThreads, attn::kSmemBytes, stream>>>(q, k, v, args);
   return cudaGetLastError();
 }
 

@@ -8,14 +8,16 @@ size_t attend_smem_bytes() { return attn::kSmemBytes; }
 cudaError_t launch_attend_kvi8r(const AttnArgs &args, cudaStream_t stream) {
   const int64_t rows = args.q_end - args.q_begin;
   if (rows <= 0 || args.heads <= 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(attn::attend_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(attn::kSmemBytes));
+  // one scale per row, or one per 32 values
+  auto kernel = args.scale_groups == 4 ? attn::attend_kernel<true, 4> : attn::attend_kernel<true, 1>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(attn::kSmemBytes));
   if (e != cudaSuccess) return e;
   CUtensorMap unused;
   memset(&unused, 0, sizeof(unused));
   const dim3 grid(static_cast<unsigned>((rows + kAttnRowsPerCta - 1) / kAttnRowsPerCta),
                   static_cast<unsigned>(args.heads));
-  attn::attend_kernel<true><<<grid, attn::kThreads, attn::kSmemBytes, stream>>>(unused, unused, unused, args);
+  kernel<<<grid, attn::kThreads, attn::kSmemBytes, stream>>>(unused, unused, unused, args);
   return cudaGetLastError();
 }
 

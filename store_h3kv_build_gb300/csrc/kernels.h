@@ -15,7 +15,8 @@ namespace h3kv {
 // outputs (box 128 x 128, 128B swizzle).
 cudaError_t launch_store_build(const CUtensorMap &k_in, const CUtensorMap &v_in, const CUtensorMap &k_out,
                                const CUtensorMap &v_out, uint16_t *k_scales, uint16_t *v_scales, int64_t rows,
-                               int num_sms, uint32_t *err, uint64_t timeout_ns, cudaStream_t stream);
+                               int num_sms, int scale_groups, uint32_t *err, uint64_t timeout_ns,
+                               cudaStream_t stream);
 size_t store_build_smem_bytes();
 
 struct AttnArgs {
@@ -41,6 +42,7 @@ struct AttnArgs {
   // keys.  stage_flags: bit 0 = first block, bit 1 = last block.
   float2 *state;
   int32_t stage_flags;
+  int32_t scale_groups;     // kvi8r scales per row: 1, or 4 (one per 32 values)
 };
 
 constexpr int kAttnRowsPerCta = 256;  // two 128-row query tiles per CTA

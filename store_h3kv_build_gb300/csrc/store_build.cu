@@ -27,7 +27,7 @@ struct BuildSmem {
   // 1024-byte aligned tiles first
   uint8_t in[kStages][kInTileBytes];
   uint8_t out_codes[2][kOutCodeBytes];
-  uint16_t out_scales[2][kRows];
+  uint16_t out_scales[2][kRows * 4];  // one fp16 scale per row, or per 32 values
   uint64_t full[kStages];
   uint64_t empty[kStages];
   int abort;
@@ -35,6 +35,33 @@ struct BuildSmem {
 
 constexpr size_t kBuildSmemBytes = sizeof(BuildSmem) + 1024;
 
+// Scale, clamp need and code multiplier of one row (or group of a row) from
+// the absmax of its unnormalised FWHT values: s = fp16(absmax(x H) / 127),
+// saturated at the largest finite fp16; codes are rne(x' / s) = rne(x * m)
+// with m = 1 / (sqrt(128) s).
+struct RowScale {
+  __half sh;
+  bool clamp;
+  float m;
+};
+__device__ __forceinline__ RowScale row_scale(float amax) {
+  RowScale rs;
+  const float a = amax * kInvSqrt128;
+  rs.sh = __float2half_rn(__fdiv_rn(a, 127.0f));
+  rs.clamp = false;
+  if (__hisinf(rs.sh)) {
+    rs.sh = __ushort_as_half(0x7BFFu);  // 65504
+    rs.clamp = true;
+  }
+  const float sf = __half2float(rs.sh);
+  rs.clamp = rs.clamp || (sf < 6.103515625e-05f);  // fp16 subnormal scale: x'/s may exceed 127.5
+  rs.m = sf > 0.f ? __frcp_rn(sf * 11.313708498984761f) : 0.f;
+  return rs;
+}
+
+// kGroups = 1: one scale per row; kGroups = 4: one per 32 consecutive
+// rotated values (the per-32-value variant).
+template <int kGroups>
 __global__ void __launch_bounds__(kThreads, 2)
     store_build_kernel(const __grid_constant__ CUtensorMap tm_k_in, const __grid_constant__ CUtensorMap tm_v_in,
                        const __grid_constant__ CUtensorMap tm_k_out, const __grid_constant__ CUtensorMap tm_v_out,
@@ -123,24 +150,28 @@ __global__ void __launch_bounds__(kThreads, 2)
 
       fwht128_packed(x);  // x now holds sqrt(128) * (row H)
 
-      float am[4] = {0.f, 0.f, 0.f, 0.f};
+      RowScale rs[kGroups];
+      if constexpr (kGroups == 1) {
+        float am[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int e = 0; e < 128; e += 8) {
+        for (int e = 0; e < 128; e += 8) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) am[u] = fmax3(am[u], fabsf(x[e + 2 * u]), fabsf(x[e + 2 * u + 1]));
+          for (int u = 0; u < 4; ++u) am[u] = fmax3(am[u], fabsf(x[e + 2 * u]), fabsf(x[e + 2 * u + 1]));
+        }
+        rs[0] = row_scale(fmax3(am[0], am[1], fmaxf(am[2], am[3])));
+      } else {
+#pragma unroll
+        for (int gi = 0; gi < kGroups; ++gi) {
+          constexpr int kW = 128 / kGroups;
+          float am[2] = {0.f, 0.f};
+#pragma unroll
+          for (int e = gi * kW; e < (gi + 1) * kW; e += 4) {
+            am[0] = fmax3(am[0], fabsf(x[e]), fabsf(x[e + 1]));
+            am[1] = fmax3(am[1], fabsf(x[e + 2]), fabsf(x[e + 3]));
+          }
+          rs[gi] = row_scale(fmaxf(am[0], am[1]));
+        }
       }
-      const float amax = fmax3(am[0], am[1], fmaxf(am[2], am[3]));
-      // s = fp16(absmax(x H) / 127), saturated at the largest finite fp16
-      const float a = amax * kInvSqrt128;
-      __half sh = __float2half_rn(__fdiv_rn(a, 127.0f));
-      bool clamp = false;
-      if (__hisinf(sh)) {
-        sh = __ushort_as_half(0x7BFFu);  // 65504
-        clamp = true;
-      }
-      const float sf = __half2float(sh);
-      clamp = clamp || (sf < 6.103515625e-05f);  // fp16 subnormal scale: x'/s may exceed 127.5
-      const float m = sf > 0.f ? __frcp_rn(sf * 11.313708498984761f) : 0.f;
 
       // code = rne(x' / s) = rne(x * m) with m = 1 / (sqrt(128) s): adding
       // 1.5 * 2^23 rounds to an integer held in the low mantissa bits, whose
@@ -154,7 +185,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int k = 0; k < 4; ++k) {
           uint32_t q[4];
           const int e = g * 16 + k * 4;
-          if (!clamp) {
+          const RowScale &gs = rs[(e * kGroups) >> 7];
+          const float m = gs.m;
+          if (!gs.clamp) {
             const float2 mm = make_float2(m, m), mg = make_float2(kMagic, kMagic);
             const float2 lo = __ffma2_rn(make_float2(x[e], x[e + 1]), mm, mg);
             const float2 hi = __ffma2_rn(make_float2(x[e + 2], x[e + 3]), mm, mg);
@@ -173,19 +206,23 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         *reinterpret_cast<uint4 *>(oc + sw128_off(r, g)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      sm.out_scales[b][r] = __half_as_ushort(sh);
+#pragma unroll
+      for (int gi = 0; gi < kGroups; ++gi) sm.out_scales[b][r * kGroups + gi] = __half_as_ushort(rs[gi].sh);
 
       const bool is_v = t >= tiles_per_tensor;
       const int64_t row0 = (is_v ? t - tiles_per_tensor : t) * kRows;
       const bool full_tile = row0 + kRows <= rows;
       uint16_t *scales = is_v ? v_scales : k_scales;
-      if (!full_tile && row0 + r < rows) scales[row0 + r] = __half_as_ushort(sh);
+      if (!full_tile && row0 + r < rows) {
+#pragma unroll
+        for (int gi = 0; gi < kGroups; ++gi) scales[(row0 + r) * kGroups + gi] = __half_as_ushort(rs[gi].sh);
+      }
 
       fence_proxy_async_smem();
       named_bar_sync(1, kRows);
       if (tid == 0) {
         tma_store_2d(is_v ? &tm_v_out : &tm_k_out, 0, static_cast<int32_t>(row0), smem_u32(oc));
-        if (full_tile) bulk_s2g(scales + row0, smem_u32(&sm.out_scales[b][0]), kRows * 2);
+        if (full_tile) bulk_s2g(scales + row0 * kGroups, smem_u32(&sm.out_scales[b][0]), kRows * kGroups * 2);
         bulk_commit();
       }
     }
@@ -200,17 +237,19 @@ size_t store_build_smem_bytes() { return kBuildSmemBytes; }
 
 cudaError_t launch_store_build(const CUtensorMap &k_in, const CUtensorMap &v_in, const CUtensorMap &k_out,
                                const CUtensorMap &v_out, uint16_t *k_scales, uint16_t *v_scales, int64_t rows,
-                               int num_sms, uint32_t *err, uint64_t timeout_ns, cudaStream_t stream) {
+                               int num_sms, int scale_groups, uint32_t *err, uint64_t timeout_ns,
+                               cudaStream_t stream) {
   static_assert(offsetof(BuildSmem, out_codes) % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
   const int64_t tiles = (rows + kRows - 1) / kRows;
   if (tiles == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(store_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kBuildSmemBytes));
+  auto kernel = scale_groups == 4 ? store_build_kernel<4> : store_build_kernel<1>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kBuildSmemBytes));
   if (e != cudaSuccess) return e;
   int64_t grid = static_cast<int64_t>(num_sms) * 2;
   if (grid > 2 * tiles) grid = 2 * tiles;
-  store_build_kernel<<<static_cast<unsigned>(grid), kThreads, kBuildSmemBytes, stream>>>(
-      k_in, v_in, k_out, v_out, k_scales, v_scales, rows, tiles, err, timeout_ns);
+  kernel<<<static_cast<unsigned>(grid), kThreads, kBuildSmemBytes, stream>>>(k_in, v_in, k_out, v_out, k_scales,
+                                                                              v_scales, rows, tiles, err, timeout_ns);
   return cudaGetLastError();
 }
 

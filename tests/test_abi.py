@@ -29,7 +29,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_abi_version_and_strings():
-    assert b.h3kv_abi_version() == 1
+    assert b.h3kv_abi_version() == 2
     for st in range(5):
         assert b.h3kv_strerror(st)
     assert b.h3kv_strerror(99) == b"unknown status"
@@ -115,3 +115,13 @@ def test_attend_staged_rejects_bad_arguments():
     assert at(4096, 256, ctypes.byref(_store(head_dim=64)), 64, 256, 0.0, 4096, 4096, big, 4096,
               None) == b.H3KV_ERR_UNSUPPORTED
     assert at(4096, 0, ctypes.byref(st), 64, 256, 0.0, 4096, 4096, big, 4096, None) == b.H3KV_OK
+
+
+def test_scale_group_validation():
+    bad = b.h3kv_store(4096, 4096, 4096, 4096, 1, 256, 128, 64)
+    assert b.h3kv_build_store(4096, 4096, 1, 256, 128, ctypes.byref(bad), None) == b.H3KV_ERR_INVALID_ARG
+    assert b.h3kv_attend(4096, 256, ctypes.byref(bad), 64, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    g32 = b.h3kv_store(4096, 4096, 4096, 4096, 1, 256, 128, 32)
+    big = b.h3kv_staging_bytes(1, 256)
+    assert b.h3kv_attend_staged(4096, 256, ctypes.byref(g32), 64, 256, 0.0, 4096, 4096, big, 4096,
+                                None) == b.H3KV_ERR_UNSUPPORTED
