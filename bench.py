@@ -168,6 +168,23 @@ def time_oracle_sample(w, rows=512, head=0, seed=0):
     return att, gbs, t2 - t0, desc
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise max of a list of timings over all ranks (a no-op without
+    an initialised process group).  Timings are the max over ranks, so the
+    slowest replica sets the whole job's throughput."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    import torch.distributed as tdist
+    if tdist.is_available() and tdist.is_initialized() and tdist.get_world_size() > 1:
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(world, units_per_rank, seconds):
+    """Whole-job throughput of `world` replicas that each processed
+    `units_per_rank` units, timed (max over ranks) at `seconds`."""
+    return world * units_per_rank / seconds
+
+
 def blas_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -261,14 +278,10 @@ def run_ours(args, w, name):
     build_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev]
     attend_ms = [e1.elapsed_time(e2) for _, e1, e2 in ev]
     total_ms = ev[0][0].elapsed_time(ev[-1][2])
-    t = torch.tensor([total_ms, sum(build_ms), sum(attend_ms)], dtype=torch.float64, device=dev)
-    if dist:
-        import torch.distributed as tdist
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-    total_ms, build_sum, attend_sum = t.tolist()
+    total_ms, build_sum, attend_sum = max_over_ranks([total_ms, sum(build_ms), sum(attend_ms)], dev)
     ms_per_step = total_ms / args.steps
     flops = attention_flops(H, L, L)
-    value = world * flops * args.steps / (total_ms / 1e3) / 1e12
+    value = job_throughput(world, flops * args.steps, total_ms / 1e3) / 1e12
 
     # ---- the exact (bf16) store on the same inputs: the pages compare kvi8r
     # attention time against it (their +16 %)
@@ -345,12 +358,8 @@ def run_ours(args, w, name):
     ee.record(stream)
     barrier()
     e2e_ms = es.elapsed_time(ee)
-    te = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-    if dist:
-        import torch.distributed as tdist
-        tdist.all_reduce(te, op=tdist.ReduceOp.MAX)
-    e2e_ms = te.item()
-    e2e_value = world * flops * e2e_steps / (e2e_ms / 1e3) / 1e12
+    e2e_ms = max_over_ranks([e2e_ms], dev)[0]
+    e2e_value = job_throughput(world, flops * e2e_steps, e2e_ms / 1e3) / 1e12
     h2d = (q.numel() + k.numel() + v.numel()) * 2
     d2h = out.numel() * 4
     b.sync_status()
