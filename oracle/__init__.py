@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for the kvi8r store and attention (test infrastructure only).
+"""fp64 CPU oracle for the kvi8r and kvf8s stores and attention (test
+infrastructure only).
 
 Only the test suite, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
 baseline / reference arm use this package.  It shares no code with the CUDA
@@ -9,3 +10,4 @@ from .kvi8r import (  # noqa: F401
     encode_rows, build_store, dequant, default_scale, softmax_attention, attend,
     attend_exact, attend_blockwise, rel_rms, group_scales, encode_rows_grouped, build_store_grouped,
 )
+from . import kvf8s  # noqa: F401
