@@ -31,12 +31,14 @@ Readings where the pages leave a step open:
       kept only as a diagnostic.
   R16 K scale: one fp32 scale per (head, 64-token block) s = absmax/448 over
       the block's smoothed values (a tail block covers the tokens it has);
-      codes = e4m3(x/s); a block with s = 0 has all codes 0.
+      codes = e4m3(x r) with r = fp32(1/s), the scale's reciprocal rounded to
+      fp32 (the encode multiplies by it); a block with s = 0 has all codes 0.
   R17 V scale: one fp32 scale per (head, channel) s = absmax/448 over all
-      tokens; codes = e4m3(v/s) with the quotient taken in fp32 (v is bf16,
-      so both sides decide every V code in the same precision).
+      tokens; codes = e4m3(v r), r = fp32(1/s), with the product taken in fp32
+      (v is bf16, so both sides decide every V code in the same precision).
   R18 Q: one fp32 scale per rotated query row, s = absmax/448, codes =
-      e4m3(q'/s); the scores are S = (code_q . code_k) s_q s_k * scale.
+      e4m3(q' r), r = fp32(1/s); the scores are
+      S = (code_q . code_k) s_q s_k * scale.
   R19 The result is exact softmax attention over the dequantised encodings
       (reading R7's blockwise combine changes nothing mathematically).  The
       fp8 P of a kernel's P.V product is a precision step of that kernel,
@@ -99,10 +101,18 @@ def fp32_round(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
 
 
+def fp32_recip(s) -> np.ndarray:
+    """fp32(1/s) of fp32 scales (1 where s = 0, never used there)."""
+    s32 = np.asarray(s, dtype=np.float64).astype(np.float32)
+    with np.errstate(divide="ignore"):
+        return np.where(s32 > 0, np.float32(1) / np.where(s32 > 0, s32, np.float32(1)), np.float32(1))
+
+
 def _scaled_codes(x: np.ndarray, s: np.ndarray) -> np.ndarray:
-    """e4m3(x / s) with s broadcast against x; all-zero codes where s = 0."""
-    safe = np.where(s > 0, s, 1.0)
-    return np.where(s > 0, e4m3_encode(x / safe), np.uint8(0)).astype(np.uint8)
+    """e4m3(x * fp32(1/s)) with s broadcast against x; all-zero codes where
+    s = 0 (readings R16, R18)."""
+    r = fp32_recip(s).astype(np.float64)
+    return np.where(s > 0, e4m3_encode(x * r), np.uint8(0)).astype(np.uint8)
 
 
 # --------------------------------------------------------------------------
@@ -142,13 +152,12 @@ def v_channel_scales(V) -> np.ndarray:
 
 def encode_v(V) -> dict:
     """V codes [heads, seq, 128] (token-major here) and fp32 per-channel
-    scales [heads, 128]; each quotient v/s in fp32 (R17)."""
+    scales [heads, 128]; each product v * fp32(1/s) in fp32 (R17)."""
     v32 = as_f64(V).astype(np.float32)
     s = v_channel_scales(V)
-    s32 = s.astype(np.float32)[:, None, :]
-    with np.errstate(divide="ignore", invalid="ignore"):
-        q = (v32 / np.where(s32 > 0, s32, np.float32(1))).astype(np.float64)
-    codes = np.where(s32 > 0, e4m3_encode(q), np.uint8(0)).astype(np.uint8)
+    r = fp32_recip(s)[:, None, :]
+    q = (v32 * r).astype(np.float64)
+    codes = np.where(s[:, None, :] > 0, e4m3_encode(q), np.uint8(0)).astype(np.uint8)
     return {"v_codes": codes, "v_scales": s}
 
 
@@ -195,7 +204,7 @@ def attend_kvf8s(Q, store: dict, scale: float | None = None, heads=None, block: 
 
 
 __all__ = [
-    "E4M3_MAX", "K_BLOCK", "HEAD_DIM", "e4m3_values", "e4m3_encode", "e4m3_decode", "fp32_round",
+    "E4M3_MAX", "K_BLOCK", "HEAD_DIM", "e4m3_values", "e4m3_encode", "e4m3_decode", "fp32_round", "fp32_recip",
     "smooth_mean", "k_block_scales", "encode_k", "v_channel_scales", "encode_v", "build_store_kvf8s",
     "dequant_k", "dequant_v", "encode_q", "attend_kvf8s",
 ]

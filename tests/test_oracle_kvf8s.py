@@ -112,13 +112,14 @@ def test_k_dequant_error_bound():
 
 def test_v_channel_scale_and_codes():
     # R17: per channel the largest |v| encodes to +-448; the codes are the
-    # fp32 quotient rounded to e4m3, which PyTorch's cast reproduces
+    # fp32 product v * fp32(1/s) rounded to e4m3, which PyTorch's fp32
+    # arithmetic and e4m3 cast reproduce
     _, _, v = synth.make_qkv(2, 100, seed=6)
     st = f8.encode_v(v)
     vv = v.float()
     s = vv.abs().amax(dim=1) / 448.0
     assert np.array_equal(st["v_scales"], s.double().numpy())
-    ref = (vv / s[:, None, :]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ref = (vv * (1.0 / s)[:, None, :]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     assert np.array_equal(st["v_codes"], ref)
     idx = vv.abs().argmax(dim=1)
     for h in range(2):
