@@ -55,6 +55,15 @@ def store_bytes(heads, seq):
     return 2 * rows * HEAD_DIM * 2 + 2 * rows * HEAD_DIM + 2 * rows * 2
 
 
+def f8_store_bytes(heads, seq):
+    """Algorithmic bytes of one kvf8s store build: bf16 K and V read twice
+    (the per-head statistics over every token must be complete before any
+    token is encoded), e4m3 codes of both written once, and the fp32 block
+    and channel scales and K means."""
+    rows = heads * seq
+    return 2 * (2 * rows * HEAD_DIM * 2) + 2 * rows * HEAD_DIM + heads * ((seq + 63) // 64) * 4 + 2 * heads * 512
+
+
 def workload_desc(name, w):
     return {
         "workload": f"{name}: {w['heads']} heads x {w['seq']} tokens x d{HEAD_DIM}, bf16 Q/K/V ~N(0,1)"
@@ -313,6 +322,23 @@ def run_ours(args, w, name):
     g32_bytes = store_bytes(H, L) + 2 * H * L * 6
     del gst
 
+    # ---- the kvf8s store (fp8 e4m3 K/V in the kvi8s layout, both products on
+    # the fp8 tensor path) on the same inputs: store build and attention
+    fst = b.StoreF8.empty(H, L, dev)
+    b.build_store_f8(k, v, out=fst)
+    b.attend_f8(q, fst, q_chunk=q_chunk, kv_block=kv_block, out=out)
+    fs, fm, fe = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    fs.record(stream)
+    b.build_store_f8(k, v, out=fst)
+    fm.record(stream)
+    b.attend_f8(q, fst, q_chunk=q_chunk, kv_block=kv_block, out=out)
+    fe.record(stream)
+    torch.cuda.synchronize(dev)
+    b.sync_status()
+    f8_build_ms, f8_attend_ms = fs.elapsed_time(fm), fm.elapsed_time(fe)
+    f8_bytes = f8_store_bytes(H, L)
+    del fst
+
     # ---- the same store held in pinned Grace memory and staged into HBM one
     # kv_block at a time (the pages keep kv_block for a host-staged K/V design)
     hst = b.Store.empty(H, L, host=True)
@@ -383,6 +409,11 @@ def run_ours(args, w, name):
             "g32_store": {"what": "one fp16 scale per 32 rotated values",
                           "attend_ms": g32_attend_ms, "attend_tflops": flops / (g32_attend_ms / 1e3) / 1e12,
                           "build_ms": g32_build_ms, "build_gbs": g32_bytes / (g32_build_ms / 1e3) / 1e9},
+            "f8_store": {"what": "kvf8s: fp8 e4m3 K/V in the kvi8s layout (rotated, mean-smoothed K with one "
+                                 "scale per 64 tokens; V per channel), both products e4m3 on the tensor cores",
+                         "attend_ms": f8_attend_ms, "attend_tflops": flops / (f8_attend_ms / 1e3) / 1e12,
+                         "build_ms": f8_build_ms, "build_bytes": f8_bytes,
+                         "build_gbs": f8_bytes / (f8_build_ms / 1e3) / 1e9},
             "host_store": {"where": "kvi8r store built into pinned Grace memory over NVLink-C2C, attended "
                                     "with h3kv_attend_staged (each kv_block copied into HBM, copies timed)",
                            "attend_ms": host_attend_ms, "attend_tflops": flops / (host_attend_ms / 1e3) / 1e12,

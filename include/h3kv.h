@@ -1,6 +1,8 @@
 /*
  * h3kv.h -- C ABI of libh3kv: the kvi8r rotated-int8 whole-sequence K/V store
- * and query-chunked attention over it, on one NVIDIA GB300 (sm_103a).
+ * and query-chunked attention over it, on one NVIDIA GB300 (sm_103a); the
+ * exact bf16 comparison path; and the kvf8s store (fp8 e4m3 in the kvi8s
+ * layout) attended on the fp8 tensor path.
  *
  * Source of the method: "H3 Streamed Blocks (exact low-VRAM, alpha)", Inputs
  * table (kv_store, q_chunk, kv_block rows), and "Low VRAM, low RAM: the
@@ -36,7 +38,7 @@
 extern "C" {
 #endif
 
-#define H3KV_ABI_VERSION 2u
+#define H3KV_ABI_VERSION 3u
 #define H3KV_HEAD_DIM 128
 /* kv_block = 0 on the kvi8r path means this many tokens (the kv_block
  * default of the kv_store row). */
@@ -169,6 +171,66 @@ h3kv_status h3kv_attend_staged(const uint16_t *Q, int64_t q_seq, const h3kv_stor
 h3kv_status h3kv_attend_staged_static(const uint16_t *Q, int64_t q_seq, const h3kv_store *store,
                                       int32_t q_chunk, int32_t kv_block, float softmax_scale, float *O,
                                       void *stream);
+
+/* ------------------------------------------------------------------ kvf8s
+ * The kvf8s store: the kvi8s layout ("The K/V store options" table of the
+ * Low VRAM write-up, kvi8s row; kv_store row of the H3 Streamed Blocks Inputs
+ * table: K with one scale per 64-token block after mean smoothing, V fp8 per
+ * channel, Q and K Hadamard-rotated, attended on the tensor cores straight
+ * from the store) with fp8 e4m3 K in place of int8, so that both attention
+ * products run on the fp8 tensor path.  e4m3 is the OCP E4M3 format (bias 7,
+ * largest finite 448); every encode rounds to nearest even and saturates.
+ *   K: k' = k H (the kvi8r basis); mu = the mean of k' over all seq tokens
+ *      (per head and channel); per (head, 64-token block)
+ *      s_k = max |k' - mu| / 448 over the block; codes e4m3((k' - mu) / s_k),
+ *      all 0 where s_k == 0.  Subtracting mu shifts every score of a query
+ *      row by the same amount, so attention does not need it; it is stored
+ *      for inspection.
+ *   V: not rotated; per (head, channel) s_v = max over all tokens |v| / 448;
+ *      codes e4m3(v / s_v) (fp32 quotient), stored channel-major (V
+ *      transposed) with a row stride of h3kv_f8_v_stride(seq) bytes; bytes
+ *      of a row past seq are 0.
+ * Every buffer is caller-owned device memory, 16-byte aligned. */
+typedef struct {
+  uint8_t *k_codes;   /* e4m3 [heads, seq, 128] */
+  uint8_t *v_codes_t; /* e4m3 [heads, 128, h3kv_f8_v_stride(seq)] */
+  float *k_scales;    /* [heads, ceil(seq / H3KV_F8_K_BLOCK)] */
+  float *v_scales;    /* [heads, 128] */
+  float *k_mean;      /* [heads, 128] */
+  int32_t heads;
+  int64_t seq;
+  int32_t head_dim;   /* must be 128 */
+} h3kv_store_f8;
+
+/* Tokens per K scale block of the kvf8s store. */
+#define H3KV_F8_K_BLOCK 64
+
+/* Row stride in bytes of the channel-major V codes: seq rounded up to a
+ * multiple of 16 (0 for seq < 0). */
+int64_t h3kv_f8_v_stride(int64_t seq);
+
+/* Bytes of a kvf8s store's five buffers together (0 for invalid arguments). */
+size_t h3kv_store_f8_bytes(int32_t heads, int64_t seq, int32_t head_dim);
+
+/* Build the kvf8s store of bf16 K and V [heads, seq, 128] into `out`, whose
+ * heads/seq/head_dim must match.  Two stream-ordered passes (statistics of
+ * every head, then the encode); every reduction runs in a fixed order, so
+ * the store is the same on every run.  heads <= 65535. */
+h3kv_status h3kv_build_store_f8(const uint16_t *K, const uint16_t *V, int32_t heads, int64_t seq,
+                                int32_t head_dim, const h3kv_store_f8 *out, void *stream);
+
+/* kvf8s attention: q' = Q H; one fp32 scale per query row s_q = max|q'|/448
+ * and e4m3 codes of q'/s_q; S = (Q codes . K codes) s_q s_k softmax_scale;
+ * P = softmax(S) over all store->seq keys (non-causal), in kv_block-token
+ * blocks combined by their log-sum-exp; O = P (V codes s_v).  V is not
+ * rotated, so O needs no un-rotation.  Both products are e4m3 x e4m3 with
+ * fp32 accumulation: the un-normalised softmax weights enter P.V as e4m3,
+ * scaled so that the largest possible weight is 448.
+ *   Q: bf16 [store->heads, q_seq, 128].  O: fp32 [store->heads, q_seq, 128].
+ *   q_chunk, kv_block and softmax_scale as for h3kv_attend; the output is
+ *   bit-identical for every q_chunk.  store->heads <= 65535. */
+h3kv_status h3kv_attend_f8(const uint16_t *Q, int64_t q_seq, const h3kv_store_f8 *store, int32_t q_chunk,
+                           int32_t kv_block, float softmax_scale, float *O, void *stream);
 
 /* Synchronise `stream`, then return and clear the device error word that the
  * kernels set when a bounded wait runs out (H3KV_ERR_DEVICE_TIMEOUT), or

@@ -42,6 +42,19 @@ class h3kv_store(ctypes.Structure):  # noqa: N801 - mirrors the C struct name
     ]
 
 
+class h3kv_store_f8(ctypes.Structure):  # noqa: N801 - mirrors the C struct name
+    _fields_ = [
+        ("k_codes", ctypes.c_void_p),
+        ("v_codes_t", ctypes.c_void_p),
+        ("k_scales", ctypes.c_void_p),
+        ("v_scales", ctypes.c_void_p),
+        ("k_mean", ctypes.c_void_p),
+        ("heads", ctypes.c_int32),
+        ("seq", ctypes.c_int64),
+        ("head_dim", ctypes.c_int32),
+    ]
+
+
 _vp, _i32, _i64, _f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
 _SIGS = {
     "h3kv_abi_version": (ctypes.c_uint32, []),
@@ -55,6 +68,10 @@ _SIGS = {
                                                  _vp]),
     "h3kv_attend_staged": (ctypes.c_int, [_vp, _i64, ctypes.POINTER(h3kv_store), _i32, _i32, _f32, _vp, _vp,
                                           ctypes.c_size_t, _vp, _vp]),
+    "h3kv_f8_v_stride": (ctypes.c_int64, [_i64]),
+    "h3kv_store_f8_bytes": (ctypes.c_size_t, [_i32, _i64, _i32]),
+    "h3kv_build_store_f8": (ctypes.c_int, [_vp, _vp, _i32, _i64, _i32, ctypes.POINTER(h3kv_store_f8), _vp]),
+    "h3kv_attend_f8": (ctypes.c_int, [_vp, _i64, ctypes.POINTER(h3kv_store_f8), _i32, _i32, _f32, _vp, _vp]),
     "h3kv_set_wait_timeout_ns": (ctypes.c_int, [ctypes.c_uint64]),
     "h3kv_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _vp]),
     "h3kv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -182,6 +199,60 @@ def attend_exact(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, q_chunk: int
     check(h3kv_attend_exact(_ptr(Q), int(Q.shape[1]), _ptr(K), _ptr(V), int(K.shape[0]), int(K.shape[1]),
                             int(K.shape[2]), int(q_chunk), int(kv_block), float(softmax_scale), _ptr(out),
                             _stream(stream)), "h3kv_attend_exact")
+    return out
+
+
+K_BLOCK_F8 = 64
+
+
+class StoreF8:
+    """A kvf8s store held in torch tensors: e4m3 K codes [heads, seq, 128]
+    (uint8), channel-major e4m3 V codes [heads, 128, v_stride], fp32 K block
+    scales [heads, ceil(seq / 64)], fp32 V channel scales and K means
+    [heads, 128]."""
+
+    def __init__(self, k_codes, v_codes_t, k_scales, v_scales, k_mean, seq: int):
+        self.k_codes, self.v_codes_t = k_codes, v_codes_t
+        self.k_scales, self.v_scales, self.k_mean = k_scales, v_scales, k_mean
+        self.heads, self.seq = int(k_codes.shape[0]), int(seq)
+
+    @classmethod
+    def empty(cls, heads: int, seq: int, device="cuda") -> "StoreF8":
+        vstride = int(h3kv_f8_v_stride(seq))
+        nblk = (seq + K_BLOCK_F8 - 1) // K_BLOCK_F8
+        kc = torch.empty((heads, seq, HEAD_DIM), dtype=torch.uint8, device=device)
+        vt = torch.empty((heads, HEAD_DIM, vstride), dtype=torch.uint8, device=device)
+        ks = torch.empty((heads, nblk), dtype=torch.float32, device=device)
+        vs = torch.empty((heads, HEAD_DIM), dtype=torch.float32, device=device)
+        km = torch.empty((heads, HEAD_DIM), dtype=torch.float32, device=device)
+        return cls(kc, vt, ks, vs, km, seq)
+
+    def c_struct(self) -> h3kv_store_f8:
+        return h3kv_store_f8(_ptr(self.k_codes), _ptr(self.v_codes_t), _ptr(self.k_scales), _ptr(self.v_scales),
+                             _ptr(self.k_mean), self.heads, self.seq, HEAD_DIM)
+
+    def nbytes(self) -> int:
+        return int(h3kv_store_f8_bytes(self.heads, self.seq, HEAD_DIM))
+
+
+def build_store_f8(K: torch.Tensor, V: torch.Tensor, out: StoreF8 | None = None, stream=None) -> StoreF8:
+    """h3kv_build_store_f8 on bf16 K, V [heads, seq, 128] (CUDA, contiguous)."""
+    heads, seq = int(K.shape[0]), int(K.shape[1])
+    out = StoreF8.empty(heads, seq, K.device) if out is None else out
+    st = out.c_struct()
+    check(h3kv_build_store_f8(_ptr(K), _ptr(V), heads, seq, int(K.shape[2]), ctypes.byref(st), _stream(stream)),
+          "h3kv_build_store_f8")
+    return out
+
+
+def attend_f8(Q: torch.Tensor, store: StoreF8, q_chunk: int = 16384, kv_block: int = 0, softmax_scale: float = 0.0,
+              out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """h3kv_attend_f8: kvf8s attention of bf16 Q [heads, q_seq, 128] -> fp32."""
+    q_seq = int(Q.shape[1])
+    out = torch.empty(Q.shape, dtype=torch.float32, device=Q.device) if out is None else out
+    st = store.c_struct()
+    check(h3kv_attend_f8(_ptr(Q), q_seq, ctypes.byref(st), int(q_chunk), int(kv_block), float(softmax_scale),
+                         _ptr(out), _stream(stream)), "h3kv_attend_f8")
     return out
 
 

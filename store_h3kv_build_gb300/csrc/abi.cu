@@ -108,6 +108,21 @@ bool encode_3d_bf16(CUtensorMap *m, const void *base, uint64_t seq, uint64_t hea
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over 8-bit codes with 128-byte rows of 128 elements along the
+// inner axis: dims {inner, mid, heads} with byte strides {mid_stride,
+// head_stride}; box 128 x 128 x 1 with the 128-byte swizzle; elements past
+// `inner` or `mid` read as zero.
+bool encode_3d_u8(CUtensorMap *m, const void *base, uint64_t inner, uint64_t mid, uint64_t heads,
+                  uint64_t mid_stride, uint64_t head_stride) {
+  const cuuint64_t dims[3] = {inner, mid, heads};
+  const cuuint64_t strides[2] = {mid_stride, head_stride};
+  const cuuint32_t box[3] = {128, 128, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // TMA coordinates are signed 32-bit; keep every row index below 2^31.
 constexpr int64_t kMaxRows = (1ll << 31) - 256;
 
@@ -342,6 +357,84 @@ h3kv_status h3kv_attend_staged(const uint16_t *Q, int64_t q_seq, const h3kv_stor
       a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
       if (h3kv::launch_attend_kvi8r(a, s) != cudaSuccess) return H3KV_ERR_CUDA;
     }
+  }
+  return H3KV_OK;
+}
+
+int64_t h3kv_f8_v_stride(int64_t seq) { return seq < 0 ? 0 : (seq + 15) / 16 * 16; }
+
+size_t h3kv_store_f8_bytes(int32_t heads, int64_t seq, int32_t head_dim) {
+  if (heads < 0 || seq < 0 || head_dim != H3KV_HEAD_DIM) return 0;
+  const size_t H = static_cast<size_t>(heads);
+  const size_t nblk = static_cast<size_t>((seq + H3KV_F8_K_BLOCK - 1) / H3KV_F8_K_BLOCK);
+  return H * static_cast<size_t>(seq) * 128 + H * 128 * static_cast<size_t>(h3kv_f8_v_stride(seq)) +
+         H * nblk * 4 + 2 * H * 128 * 4;
+}
+
+h3kv_status h3kv_build_store_f8(const uint16_t *K, const uint16_t *V, int32_t heads, int64_t seq,
+                                int32_t head_dim, const h3kv_store_f8 *out, void *stream) {
+  if (heads < 0 || seq < 0 || !out) return H3KV_ERR_INVALID_ARG;
+  if (head_dim != H3KV_HEAD_DIM || out->head_dim != H3KV_HEAD_DIM) return H3KV_ERR_UNSUPPORTED;
+  if (out->heads != heads || out->seq != seq) return H3KV_ERR_INVALID_ARG;
+  const int64_t rows = static_cast<int64_t>(heads) * seq;
+  if (rows == 0) return H3KV_OK;
+  if (rows > kMaxRows || heads > 65535) return H3KV_ERR_INVALID_ARG;
+  if (!K || !V || !out->k_codes || !out->v_codes_t || !out->k_scales || !out->v_scales || !out->k_mean)
+    return H3KV_ERR_INVALID_ARG;
+  if (!aligned16(K) || !aligned16(V) || !aligned16(out->k_codes) || !aligned16(out->v_codes_t) ||
+      !aligned16(out->k_scales) || !aligned16(out->v_scales) || !aligned16(out->k_mean))
+    return H3KV_ERR_INVALID_ARG;
+  DeviceInfo *d = nullptr;
+  h3kv_status st = device_info(&d);
+  if (st != H3KV_OK) return st;
+  const cudaError_t e = h3kv::launch_store_build_f8(K, V, heads, seq, h3kv_f8_v_stride(seq), out->k_codes,
+                                                    out->v_codes_t, out->k_scales, out->v_scales, out->k_mean,
+                                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? H3KV_OK : H3KV_ERR_CUDA;
+}
+
+h3kv_status h3kv_attend_f8(const uint16_t *Q, int64_t q_seq, const h3kv_store_f8 *store, int32_t q_chunk,
+                           int32_t kv_block, float softmax_scale, float *O, void *stream) {
+  if (!store || q_seq < 0 || store->heads < 0 || store->seq < 0) return H3KV_ERR_INVALID_ARG;
+  if (store->head_dim != H3KV_HEAD_DIM) return H3KV_ERR_UNSUPPORTED;
+  h3kv_status st = check_chunks(q_chunk, kv_block);
+  if (st != H3KV_OK) return st;
+  if (store->heads == 0 || q_seq == 0) return H3KV_OK;
+  if (store->seq == 0 || store->heads > 65535) return H3KV_ERR_INVALID_ARG;
+  const int64_t H = store->heads;
+  if (H * q_seq > kMaxRows || H * store->seq > kMaxRows) return H3KV_ERR_INVALID_ARG;
+  if (!Q || !O || !store->k_codes || !store->v_codes_t || !store->k_scales || !store->v_scales)
+    return H3KV_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(O) || !aligned16(store->k_codes) || !aligned16(store->v_codes_t) ||
+      !aligned16(store->k_scales) || !aligned16(store->v_scales))
+    return H3KV_ERR_INVALID_ARG;
+  DeviceInfo *d = nullptr;
+  st = device_info(&d);
+  if (st != H3KV_OK) return st;
+  const uint64_t L = static_cast<uint64_t>(store->seq);
+  const uint64_t vs = static_cast<uint64_t>(h3kv_f8_v_stride(store->seq));
+  CUtensorMap tk, tv;
+  if (!encode_3d_u8(&tk, store->k_codes, 128, L, static_cast<uint64_t>(H), 128, L * 128) ||
+      !encode_3d_u8(&tv, store->v_codes_t, L, 128, static_cast<uint64_t>(H), vs, 128 * vs))
+    return H3KV_ERR_CUDA;
+  const int32_t kvb = kv_block == 0 ? H3KV_DEFAULT_KV_BLOCK : kv_block;
+  h3kv::F8Args a{};
+  a.q = Q;
+  a.o = O;
+  a.k_scales = store->k_scales;
+  a.v_scales = store->v_scales;
+  a.q_seq = q_seq;
+  a.kv_seq = store->seq;
+  a.heads = store->heads;
+  a.kv_block_tiles = kvb / H3KV_KV_TILE;
+  a.k_blocks = static_cast<int32_t>((store->seq + H3KV_F8_K_BLOCK - 1) / H3KV_F8_K_BLOCK);
+  a.scale_log2 = scale_log2_of(softmax_scale);
+  a.err = d->err;
+  a.timeout_ns = g_timeout_ns.load();
+  for (int64_t c0 = 0; c0 < q_seq; c0 += q_chunk) {
+    a.q_begin = c0;
+    a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
+    if (h3kv::launch_attend_f8(tk, tv, a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return H3KV_ERR_CUDA;
   }
   return H3KV_OK;
 }

@@ -52,6 +52,37 @@ constexpr int kAttnRowsPerCta = 256;  // two 128-row query tiles per CTA
 // box 64 x 128 x 1, 128B swizzle); the kvi8r path reads Q with plain loads
 // and the store with bulk copies (the maps are unused).
 cudaError_t launch_attend_kvi8r(const AttnArgs &args, cudaStream_t stream);
+
+// kvf8s store build: statistics pass (K mean, V channel absmax) then the
+// encode pass.  V codes are written channel-major with row stride v_stride
+// (a multiple of 16, >= seq).
+cudaError_t launch_store_build_f8(const uint16_t *K, const uint16_t *V, int32_t heads, int64_t seq, int64_t v_stride,
+                                  uint8_t *k_codes, uint8_t *v_codes_t, float *k_scales, float *v_scales,
+                                  float *k_mean, cudaStream_t stream);
+
+struct F8Args {
+  const uint16_t *q;        // bf16 [heads, q_seq, 128]
+  float *o;                 // fp32 [heads, q_seq, 128]
+  const float *k_scales;    // [heads, k_blocks], one per 64 keys
+  const float *v_scales;    // [heads, 128], one per channel
+  int64_t q_seq;
+  int64_t kv_seq;
+  int64_t q_begin;          // this launch's query chunk [q_begin, q_end)
+  int64_t q_end;
+  int32_t heads;
+  int32_t kv_block_tiles;   // 128-key tiles per kv_block
+  int32_t k_blocks;         // ceil(kv_seq / 64)
+  float scale_log2;         // softmax_scale * log2(e)
+  uint32_t *err;
+  uint64_t timeout_ns;
+};
+
+// kvf8s attention over [q_begin, q_end): K codes through a 3-D map {128,
+// seq, heads} and channel-major V codes through {seq, 128, heads}, both u8,
+// box 128 x 128 x 1, 128B swizzle.
+cudaError_t launch_attend_f8(const CUtensorMap &k_codes, const CUtensorMap &v_codes_t, const F8Args &args,
+                             cudaStream_t stream);
+size_t attend_f8_smem_bytes();
 cudaError_t launch_attend_exact(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                                 const AttnArgs &args, cudaStream_t stream);
 size_t attend_smem_bytes();

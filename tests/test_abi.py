@@ -29,7 +29,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_abi_version_and_strings():
-    assert b.h3kv_abi_version() == 2
+    assert b.h3kv_abi_version() == 3
     for st in range(5):
         assert b.h3kv_strerror(st)
     assert b.h3kv_strerror(99) == b"unknown status"
@@ -125,3 +125,43 @@ def test_scale_group_validation():
     big = b.h3kv_staging_bytes(1, 256)
     assert b.h3kv_attend_staged(4096, 256, ctypes.byref(g32), 64, 256, 0.0, 4096, 4096, big, 4096,
                                 None) == b.H3KV_ERR_UNSUPPORTED
+
+
+def test_store_f8_sizes():
+    assert b.h3kv_f8_v_stride(0) == 0 and b.h3kv_f8_v_stride(1) == 16 and b.h3kv_f8_v_stride(217088) == 217088
+    assert b.h3kv_f8_v_stride(77) == 80 and b.h3kv_f8_v_stride(-5) == 0
+    H, L = 32, 217088
+    assert b.h3kv_store_f8_bytes(H, L, 128) == H * L * 128 * 2 + H * (L // 64) * 4 + 2 * H * 128 * 4
+    assert b.h3kv_store_f8_bytes(1, 77, 128) == 77 * 128 + 128 * 80 + 2 * 4 + 2 * 128 * 4
+    assert b.h3kv_store_f8_bytes(1, 10, 64) == 0 and b.h3kv_store_f8_bytes(-1, 10, 128) == 0
+
+
+def _store_f8(heads=1, seq=256, ptr=4096, head_dim=128):
+    return b.h3kv_store_f8(ptr, ptr, ptr, ptr, ptr, heads, seq, head_dim)
+
+
+def test_build_store_f8_rejects_bad_arguments():
+    st = _store_f8()
+    bs = b.h3kv_build_store_f8
+    assert bs(4096, 4096, 1, 256, 128, None, None) == b.H3KV_ERR_INVALID_ARG
+    assert bs(4096, 4096, 1, 256, 64, ctypes.byref(st), None) == b.H3KV_ERR_UNSUPPORTED
+    assert bs(4096, 4096, 2, 256, 128, ctypes.byref(st), None) == b.H3KV_ERR_INVALID_ARG   # shape mismatch
+    assert bs(0, 4096, 1, 256, 128, ctypes.byref(st), None) == b.H3KV_ERR_INVALID_ARG      # null K
+    assert bs(4100, 4096, 1, 256, 128, ctypes.byref(st), None) == b.H3KV_ERR_INVALID_ARG   # misaligned
+    assert bs(4096, 4096, 1, 256, 128, ctypes.byref(_store_f8(ptr=0)), None) == b.H3KV_ERR_INVALID_ARG
+    big = _store_f8(heads=70000, seq=1)
+    assert bs(4096, 4096, 70000, 1, 128, ctypes.byref(big), None) == b.H3KV_ERR_INVALID_ARG  # grid limit
+    assert bs(0, 0, 0, 0, 128, ctypes.byref(_store_f8(heads=0, seq=0, ptr=0)), None) == b.H3KV_OK
+
+
+def test_attend_f8_rejects_bad_arguments():
+    st = _store_f8()
+    at = b.h3kv_attend_f8
+    assert at(4096, 256, None, 256, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    assert at(4096, 256, ctypes.byref(st), 0, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG      # q_chunk 0
+    assert at(4096, 256, ctypes.byref(st), 64, 100, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG   # kv_block % 128
+    assert at(4096, 256, ctypes.byref(_store_f8(head_dim=64)), 64, 0, 0.0, 4096, None) == b.H3KV_ERR_UNSUPPORTED
+    assert at(4104, 256, ctypes.byref(st), 64, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG     # misaligned Q
+    assert at(4096, 256, ctypes.byref(st), 64, 0, 0.0, 0, None) == b.H3KV_ERR_INVALID_ARG        # null O
+    assert at(4096, 256, ctypes.byref(_store_f8(seq=0)), 64, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    assert at(4096, 0, ctypes.byref(st), 64, 0, 0.0, 4096, None) == b.H3KV_OK

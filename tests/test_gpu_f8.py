@@ -1,0 +1,259 @@
+"""GPU parity of the kvf8s store build and attention (h3kv_build_store_f8,
+h3kv_attend_f8) against the fp64 oracle (``oracle.kvf8s``).
+
+The store is kvi8s's layout with fp8 e4m3 K ("The K/V store options" table
+of the Low VRAM write-up, kvi8s row): rotated, mean-smoothed K with one scale
+per 64-token block; V with one scale per channel, stored channel-major.
+
+Bars:
+  * V codes and V scales: bit-exact (both sides divide bf16 values by the
+    same fp32 scale in fp32 and round to e4m3);
+  * K codes: identical except at most 1e-3 of them, each on a neighbouring
+    e4m3 value (the GPU rotates and smooths in fp32, the oracle in fp64);
+    K scales within 4 fp32 ulp; K means within 1e-5 (1 + max |k'|) of the
+    head (fp32 sums over the sequence);
+  * attention: the GPU's P.V takes the un-normalised softmax weights as e4m3
+    (scaled so the largest possible weight is 448 = 56 * 2^3), so against the
+    oracle's exact softmax over the same store each output element may be off
+    by at most
+        B = 2^-4 sum_j p_j |v_j| + 2^-10 sum_j |v_j| / (56 Z)
+    (relative rounding of normal weights + absolute rounding of subnormal
+    ones; p the normalised softmax, Z = sum_j exp(s_j - max s)), plus 2e-3
+    for fp32 accumulation and the rare query code that the fp32 and fp64
+    rotations round differently; the mean error must stay below a quarter of
+    the mean bound (the rounding errors are unbiased and average out).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import kvf8s as f8
+from store_h3kv_build_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+K_CODE_MISMATCH_FRAC = 1e-3
+SLACK = 2e-3
+
+
+def _b():
+    from store_h3kv_build_gb300 import binding as b
+    return b
+
+
+def _build(K, V):
+    b = _b()
+    st = b.build_store_f8(K, V)
+    b.sync_status()
+    return st
+
+
+def gpu_store_numpy(st, heads=None):
+    """GPU kvf8s store -> the oracle's dict layout (V back to token-major)."""
+    idx = list(range(st.heads)) if heads is None else list(heads)
+    L = st.seq
+    return {
+        "k_codes": st.k_codes[idx].cpu().numpy(),
+        "k_scales": st.k_scales[idx].cpu().double().numpy(),
+        "k_mean": st.k_mean[idx].cpu().double().numpy(),
+        "v_codes": st.v_codes_t[idx][:, :, :L].transpose(1, 2).contiguous().cpu().numpy(),
+        "v_scales": st.v_scales[idx].cpu().double().numpy(),
+    }
+
+
+def compare_k_codes(g, r, what):
+    g = g.astype(np.int16)
+    r = r.astype(np.int16)
+    bad = g != r
+    frac = float(bad.mean()) if bad.size else 0.0
+    assert frac <= K_CODE_MISMATCH_FRAC, f"{what}: {frac:.2e} of K codes differ"
+    if bad.any():
+        gv = f8.e4m3_decode(g[bad].astype(np.uint8))
+        rv = f8.e4m3_decode(r[bad].astype(np.uint8))
+        # neighbouring values: same sign (or zero), magnitude codes one apart
+        mg, mr = g[bad] & 0x7F, r[bad] & 0x7F
+        assert np.all(np.abs(mg - mr) <= 1), f"{what}: K code off by more than one step"
+        assert np.all((np.sign(gv) == np.sign(rv)) | (gv == 0) | (rv == 0)), f"{what}: sign flip"
+    return frac
+
+
+def check_store(st, K, V, heads=None, what=""):
+    heads = list(range(K.shape[0])) if heads is None else heads
+    g = gpu_store_numpy(st, heads)
+    ref = f8.build_store_kvf8s(K[heads], V[heads])
+    # V: bit-exact
+    assert np.array_equal(g["v_scales"], ref["v_scales"]), f"{what}: V scales"
+    assert np.array_equal(g["v_codes"], ref["v_codes"]), f"{what}: V codes"
+    # V padding past seq is zero
+    pad = st.v_codes_t[heads][:, :, st.seq:]
+    assert not pad.any(), f"{what}: V padding"
+    # K
+    # fp32 sums over the sequence: relative to the largest rotated value
+    kr_max = np.abs(oracle.rotate(K[heads])).max(axis=(1, 2))[:, None]
+    assert np.all(np.abs(g["k_mean"] - ref["k_mean"]) <= 1e-5 * (1.0 + kr_max)), f"{what}: K mean"
+    rs = ref["k_scales"]
+    ulp = np.abs(g["k_scales"].astype(np.float32).view(np.int32).astype(np.int64) -
+                 rs.astype(np.float32).view(np.int32).astype(np.int64))
+    assert ulp.max(initial=0) <= 4, f"{what}: K scale off by {ulp.max()} ulp"
+    return compare_k_codes(g["k_codes"], ref["k_codes"], what)
+
+
+def error_bound(Q, store, scale=None):
+    """Per-element bound B [heads, q_seq, 128] of the e4m3 rounding of P, from
+    the oracle's exact softmax over the same store."""
+    Q = oracle.as_f64(Q)
+    scale = oracle.default_scale() if scale is None else scale
+    qc, qs = f8.encode_q(Q)
+    out = np.empty(Q.shape)
+    for h in range(Q.shape[0]):
+        qd = f8.e4m3_decode(qc[h]) * qs[h][:, None]
+        kd = f8.dequant_k(store, h)
+        av = np.abs(f8.dequant_v(store, h))
+        s = (qd @ kd.T) * scale
+        e = np.exp(s - s.max(axis=1, keepdims=True))
+        Z = e.sum(axis=1, keepdims=True)
+        out[h] = 2.0 ** -4 * (e @ av) / Z + 2.0 ** -10 * av.sum(axis=0)[None, :] / (56.0 * Z)
+    return out
+
+
+def compare_f8_attention(out, Q, store, what="", rows=None):
+    """GPU output vs the oracle over the same store within the bound."""
+    ref = f8.attend_kvf8s(Q, store)
+    B = error_bound(Q, store)
+    g = out.detach().cpu().double().numpy()
+    assert np.isfinite(g).all(), f"{what}: non-finite"
+    err = np.abs(g - ref)
+    worst = float((err - B - SLACK).max())
+    assert worst <= 0, f"{what}: error exceeds the bound by {worst:.3e} (max err {err.max():.3e})"
+    assert err.mean() <= 0.25 * B.mean(), f"{what}: mean error {err.mean():.3e} vs mean bound {B.mean():.3e}"
+    return float(err.max()), float(err.mean()), float(B.mean())
+
+
+# ------------------------------------------------------------------ store --
+def test_store_f8_tiny(cuda):
+    q, k, v = synth.make_qkv(1, 1024, seed=0)
+    st = _build(k.to(cuda), v.to(cuda))
+    check_store(st, k, v, what="tiny")
+
+
+@pytest.mark.parametrize("heads,seq", [(3, 1000), (1, 1), (2, 129), (5, 77), (2, 64), (1, 8192)])
+def test_store_f8_ragged(cuda, heads, seq):
+    q, k, v = synth.make_qkv(heads, seq, seed=4, k_outliers=True)
+    st = _build(k.to(cuda), v.to(cuda))
+    check_store(st, k, v, what=f"{heads}x{seq}")
+
+
+def test_store_f8_special_rows(cuda):
+    # zero rows and a zero 64-token block, a block of one huge row, constant
+    # V channels, a V channel that is all zero
+    k = synth.normal_f32((1, 300, 128), 9)
+    k[0, 64:128] = 0                 # one all-zero block (before smoothing)
+    k[0, 130] *= 1e4
+    kb = k.to(torch.bfloat16)
+    v = synth.normal_f32((1, 300, 128), 10)
+    v[0, :, 5] = 0.0
+    v[0, :, 6] = 3.0
+    vb = v.to(torch.bfloat16)
+    st = _build(kb.to(cuda), vb.to(cuda))
+    check_store(st, kb, vb, what="special")
+    assert float(st.v_scales[0, 5]) == 0.0 and not st.v_codes_t[0, 5].any()
+    assert bool((st.v_codes_t[0, 6, :300] == 0x7E).all())
+
+
+def test_store_f8_deterministic(cuda):
+    q, k, v = synth.make_qkv(4, 5000, seed=12, k_outliers=True, device=cuda)
+    a, b2 = _build(k, v), _build(k, v)
+    for name in ("k_codes", "v_codes_t", "k_scales", "v_scales", "k_mean"):
+        assert torch.equal(getattr(a, name), getattr(b2, name)), name
+
+
+def test_store_f8_h24_l32768_outlier(cuda):
+    w = synth.WORKLOADS["h24_l32768_outlier"]
+    q, k, v = synth.make_qkv(w["heads"], w["seq"], seed=0, k_outliers=True)
+    st = _build(k.to(cuda), v.to(cuda))
+    check_store(st, k, v, heads=[0, 7, 23], what="h24 l32768")
+
+
+# -------------------------------------------------------------- attention --
+@pytest.mark.parametrize("q_chunk,kv_block", [(256, 512), (1024, 0), (100, 128), (1, 256)])
+def test_attend_f8_tiny(cuda, q_chunk, kv_block):
+    b = _b()
+    q, k, v = synth.make_qkv(1, 1024, seed=0)
+    st = _build(k.to(cuda), v.to(cuda))
+    out = b.attend_f8(q.to(cuda), st, q_chunk=q_chunk, kv_block=kv_block)
+    b.sync_status()
+    compare_f8_attention(out, q, gpu_store_numpy(st), f"tiny q_chunk={q_chunk} kv_block={kv_block}")
+
+
+@pytest.mark.parametrize("heads,q_seq,kv_seq,q_chunk,kv_block",
+                         [(2, 1000, 1337, 300, 512), (1, 1, 1, 1, 0), (3, 129, 5, 64, 128),
+                          (1, 700, 4000, 700, 1024), (2, 257, 300, 257, 0), (1, 300, 65, 128, 0)])
+def test_attend_f8_ragged(cuda, heads, q_seq, kv_seq, q_chunk, kv_block):
+    b = _b()
+    q, k, v = synth.make_qkv(heads, kv_seq, seed=7, q_seq=q_seq, k_outliers=True)
+    st = _build(k.to(cuda), v.to(cuda))
+    out = b.attend_f8(q.to(cuda), st, q_chunk=q_chunk, kv_block=kv_block)
+    b.sync_status()
+    compare_f8_attention(out, q, gpu_store_numpy(st), f"{heads}x{q_seq}x{kv_seq}")
+
+
+def test_attend_f8_q_chunk_invariance(cuda):
+    # the q_chunk row: exact at any value -> bit-identical outputs
+    b = _b()
+    q, k, v = synth.make_qkv(2, 3000, seed=3, k_outliers=True, device=cuda)
+    st = _build(k, v)
+    outs = [b.attend_f8(q, st, q_chunk=c, kv_block=1024) for c in (3000, 1024, 700, 256)]
+    b.sync_status()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
+def test_attend_f8_zero_queries_average_v(cuda):
+    # q = 0: uniform weights -> the mean of the dequantised V, in the original basis
+    b = _b()
+    _, k, v = synth.make_qkv(1, 777, seed=8)
+    q = torch.zeros((1, 40, 128), dtype=torch.bfloat16)
+    st = _build(k.to(cuda), v.to(cuda))
+    out = b.attend_f8(q.to(cuda), st)
+    b.sync_status()
+    ref = f8.dequant_v(gpu_store_numpy(st), 0).mean(axis=0)
+    # every weight is 56 * 2^0 = 56, exact in e4m3
+    assert np.max(np.abs(out[0].cpu().double().numpy() - ref[None, :])) < 1e-5
+
+
+def test_attend_f8_h24_l32768_sampled(cuda):
+    # the q_chunk=16384, kv_block=16384 launch configuration on the outlier
+    # workload; sampled heads in full
+    b = _b()
+    w = synth.WORKLOADS["h24_l32768_outlier"]
+    q, k, v = synth.make_qkv(w["heads"], w["seq"], seed=0, k_outliers=True, device=cuda)
+    st = _build(k, v)
+    out = b.attend_f8(q, st, q_chunk=16384, kv_block=16384)
+    b.sync_status()
+    heads = [0, 11]
+    rows = torch.arange(0, w["seq"], 97)
+    qs = q[heads][:, rows].cpu()
+    compare_f8_attention(out[heads][:, rows], qs, gpu_store_numpy(st, heads), "h24 l32768 sampled")
+
+
+@pytest.mark.slow
+def test_f8_full_size_h32_l217088(cuda):
+    # the full-size workload in the launch configuration the bench times:
+    # store heads 0 and 31 in full; attention on 64 sampled rows x 8 heads
+    b = _b()
+    w = synth.WORKLOADS["h32_l217088_outlier"]
+    q, k, v = synth.make_qkv(w["heads"], w["seq"], seed=0, k_outliers=True, device=cuda)
+    st = _build(k, v)
+    kc, vc = k.cpu(), v.cpu()
+    for h in (0, 31):
+        g = gpu_store_numpy(st, [h])
+        ref = f8.build_store_kvf8s(kc[h:h + 1], vc[h:h + 1])
+        assert np.array_equal(g["v_codes"], ref["v_codes"]) and np.array_equal(g["v_scales"], ref["v_scales"])
+        compare_k_codes(g["k_codes"], ref["k_codes"], f"h{h}")
+    out = b.attend_f8(q, st, q_chunk=16384, kv_block=16384)
+    b.sync_status()
+    heads = [0, 5, 9, 13, 17, 21, 26, 31]
+    rows = torch.linspace(0, w["seq"] - 1, 64).long()
+    compare_f8_attention(out[heads][:, rows], q[heads][:, rows].cpu(), gpu_store_numpy(st, heads),
+                         "h32 l217088 sampled")
