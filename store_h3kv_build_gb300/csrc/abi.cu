@@ -389,7 +389,7 @@ h3kv_status h3kv_build_store_f8(const uint16_t *K, const uint16_t *V, int32_t he
   if (st != H3KV_OK) return st;
   const cudaError_t e = h3kv::launch_store_build_f8(K, V, heads, seq, h3kv_f8_v_stride(seq), out->k_codes,
                                                     out->v_codes_t, out->k_scales, out->v_scales, out->k_mean,
-                                                    static_cast<cudaStream_t>(stream));
+                                                    d->err, g_timeout_ns.load(), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? H3KV_OK : H3KV_ERR_CUDA;
 }
 

@@ -58,7 +58,7 @@ cudaError_t launch_attend_kvi8r(const AttnArgs &args, cudaStream_t stream);
 // (a multiple of 16, >= seq).
 cudaError_t launch_store_build_f8(const uint16_t *K, const uint16_t *V, int32_t heads, int64_t seq, int64_t v_stride,
                                   uint8_t *k_codes, uint8_t *v_codes_t, float *k_scales, float *v_scales,
-                                  float *k_mean, cudaStream_t stream);
+                                  float *k_mean, uint32_t *err, uint64_t timeout_ns, cudaStream_t stream);
 
 struct F8Args {
   const uint16_t *q;        // bf16 [heads, q_seq, 128]

@@ -23,7 +23,7 @@ namespace cg = cooperative_groups;
 namespace h3kv {
 namespace f8store {
 
-constexpr int kStatCtas = 8;      // one cluster of CTAs per head
+constexpr int kStatCtas = 16;     // one cluster of CTAs per head (8 where 16 cannot launch)
 constexpr int kStatThreads = 512;
 constexpr int kStatUnroll = 4;    // row pairs per warp in flight
 constexpr int kStatWarps = kStatThreads / 32;
@@ -38,13 +38,13 @@ __device__ __forceinline__ void bf16x4(const uint2 w, float (&x)[4]) {
   x[3] = bf16hi_to_f32(w.y);
 }
 
-// Pass 1, grid (kStatCtas, heads), one cluster per head.  CTA r sums the
-// tokens [r * per, (r + 1) * per).  Each warp reads two rows per load
+// Pass 1, grid (cluster size, heads), one cluster per head.  CTA r of n sums
+// the tokens [r * per, (r + 1) * per), per = ceil(seq / n).  Each warp reads two rows per load
 // (half-warp = row, lane = 8 channels, 16-byte loads), kStatUnroll pairs at
 // a time, stepping over the range by the CTA's warps.  Partials are combined
 // half-warp, warp, then CTA by CTA through distributed shared memory, always
 // in index order, so the result does not depend on timing.
-__global__ void __cluster_dims__(kStatCtas, 1, 1) __launch_bounds__(kStatThreads)
+__global__ void __launch_bounds__(kStatThreads)
     stats_kernel(const uint16_t *K, const uint16_t *V, int64_t seq, float *k_mean, float *v_scales) {
   __shared__ float part_sum[kStatWarps][128];
   __shared__ float part_max[kStatWarps][128];
@@ -52,10 +52,11 @@ __global__ void __cluster_dims__(kStatCtas, 1, 1) __launch_bounds__(kStatThreads
   __shared__ float cta_max[128];
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
+  const int nc = static_cast<int>(cluster.num_blocks());
   const int h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = lane >> 4, l16 = lane & 15;
-  const int64_t per = (seq + kStatCtas - 1) / kStatCtas;
+  const int64_t per = (seq + nc - 1) / nc;
   const int64_t r0 = rank * per;
   const int64_t r1 = r0 + per < seq ? r0 + per : seq;
   const uint16_t *kh = K + static_cast<int64_t>(h) * seq * 128 + 8 * l16;
@@ -113,7 +114,7 @@ __global__ void __cluster_dims__(kStatCtas, 1, 1) __launch_bounds__(kStatThreads
   cluster.sync();
   if (rank == 0 && warp == 0) {
     float x[4] = {0.f, 0.f, 0.f, 0.f}, mx[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int q = 0; q < kStatCtas; ++q) {
+    for (int q = 0; q < nc; ++q) {
       const float *ps = cluster.map_shared_rank(cta_sum, q);
       const float *pm = cluster.map_shared_rank(cta_max, q);
 #pragma unroll
@@ -154,31 +155,68 @@ __device__ __forceinline__ void transpose4x4(uint32_t a, uint32_t b, uint32_t e,
   out[3] = __byte_perm(t1, t3, 0x7632);
 }
 
-// Pass 2, grid (blocks of 64 tokens, heads), 4 warps.  Warp w takes tokens
-// 16w .. 16w+15 of the block, one token at a time across the warp (lane l:
-// channels 4l .. 4l+3).
+struct EncSmem {
+  uint8_t k[kBlockTok * 256];  // the block's bf16 K rows
+  uint8_t v[kBlockTok * 256];  // and V rows
+  uint64_t full;
+  float warp_amax[kEncThreads / 32];
+  int abort;
+};
+
+// Pass 2, grid (blocks of 64 tokens, heads), 4 warps.  One bulk copy each
+// brings the block's K and V rows (contiguous within the head) into shared
+// memory; warp w then takes tokens 16w .. 16w+15, one token at a time across
+// the warp (lane l: channels 4l .. 4l+3).
 __global__ void __launch_bounds__(kEncThreads)
     encode_kernel(const uint16_t *K, const uint16_t *V, int64_t seq, int64_t v_stride, const float *k_mean,
-                  const float *v_scales, uint8_t *k_codes, float *k_scales, uint8_t *v_codes_t) {
-  __shared__ float warp_amax[kEncThreads / 32];
+                  const float *v_scales, uint8_t *k_codes, float *k_scales, uint8_t *v_codes_t, uint32_t *err,
+                  uint64_t timeout_ns) {
+  __shared__ __align__(128) EncSmem sm;
   const int h = blockIdx.y;
   const int64_t blk = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t tok0 = blk * kBlockTok + warp * 16;
+  const int64_t blk0 = blk * kBlockTok;
+  const int64_t tok0 = blk0 + warp * 16;
   const int64_t nblk = (seq + kBlockTok - 1) / kBlockTok;
   const int64_t base = static_cast<int64_t>(h) * seq;
+  const int valid = static_cast<int>(seq - blk0 < kBlockTok ? seq - blk0 : kBlockTok);
+  const uint32_t bar = smem_u32(&sm.full);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    sm.abort = 0;
+    fence_mbar_init();
+    const uint32_t bytes = static_cast<uint32_t>(valid) * 256u;
+    mbar_arrive_expect_tx(bar, 2 * bytes);
+    bulk_g2s(smem_u32(sm.k), K + (base + blk0) * 128, bytes, bar);
+    bulk_g2s(smem_u32(sm.v), V + (base + blk0) * 128, bytes, bar);
+  }
+  // per-head constants load while the copies are in flight
+  float mu[4], rv[4];
+  uint32_t keep = 0u;  // byte mask of the V channels with a nonzero scale
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    mu[c] = k_mean[static_cast<int64_t>(h) * 128 + 4 * lane + c];
+    const float sv = v_scales[static_cast<int64_t>(h) * 128 + 4 * lane + c];
+    rv[c] = sv > 0.f ? __frcp_rn(sv) : 0.f;
+    keep |= (sv > 0.f ? 0xFFu : 0u) << (8 * c);
+  }
+  __syncthreads();
+  const WaitCtx wctx{err, &sm.abort, timeout_ns};
+  if (!__syncthreads_and(mbar_wait(bar, 0, wctx))) {
+    // the copies must land before the CTA exits
+    if (threadIdx.x == 0) mbar_wait_drain(bar, 0, kDrainNs);
+    return;
+  }
 
   // ---- K: rotate, smooth, block absmax, encode
-  float mu[4];
-#pragma unroll
-  for (int c = 0; c < 4; ++c) mu[c] = k_mean[static_cast<int64_t>(h) * 128 + 4 * lane + c];
   float x[16][4];
   float amax = 0.f;
 #pragma unroll
   for (int t = 0; t < 16; ++t) {
-    const int64_t tok = tok0 + t;
-    if (tok < seq) {
-      bf16x4(*reinterpret_cast<const uint2 *>(K + (base + tok) * 128 + 4 * lane), x[t]);
+    const int lr = warp * 16 + t;
+    if (lr < valid) {
+      bf16x4(*reinterpret_cast<const uint2 *>(sm.k + lr * 256 + 8 * lane), x[t]);
       fwht128_warp(x[t], lane);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -190,9 +228,9 @@ __global__ void __launch_bounds__(kEncThreads)
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  if (lane == 0) warp_amax[warp] = amax;
+  if (lane == 0) sm.warp_amax[warp] = amax;
   __syncthreads();
-  const float bmax = fmaxf(fmaxf(warp_amax[0], warp_amax[1]), fmaxf(warp_amax[2], warp_amax[3]));
+  const float bmax = fmaxf(fmaxf(sm.warp_amax[0], sm.warp_amax[1]), fmaxf(sm.warp_amax[2], sm.warp_amax[3]));
   const float s = __fdiv_rn(bmax, kE4m3Max);
   const float rs = s > 0.f ? __frcp_rn(s) : 0.f;
   if (threadIdx.x == 0) k_scales[static_cast<int64_t>(h) * nblk + blk] = s;
@@ -203,22 +241,14 @@ __global__ void __launch_bounds__(kEncThreads)
   }
 
   // ---- V: per-channel scales, encode, write transposed
-  float rv[4];
-  uint32_t keep = 0u;  // byte mask of the channels with a nonzero scale
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const float sv = v_scales[static_cast<int64_t>(h) * 128 + 4 * lane + c];
-    rv[c] = sv > 0.f ? __frcp_rn(sv) : 0.f;
-    keep |= (sv > 0.f ? 0xFFu : 0u) << (8 * c);
-  }
   uint32_t w[16];
 #pragma unroll
   for (int t = 0; t < 16; ++t) {
-    const int64_t tok = tok0 + t;
+    const int lr = warp * 16 + t;
     w[t] = 0u;
-    if (tok < seq) {
+    if (lr < valid) {
       float v[4];
-      bf16x4(*reinterpret_cast<const uint2 *>(V + (base + tok) * 128 + 4 * lane), v);
+      bf16x4(*reinterpret_cast<const uint2 *>(sm.v + lr * 256 + 8 * lane), v);
       w[t] = pack_e4m3x4(__fmul_rn(v[0], rv[0]), __fmul_rn(v[1], rv[1]), __fmul_rn(v[2], rv[2]),
                          __fmul_rn(v[3], rv[3])) & keep;
     }
@@ -246,15 +276,39 @@ __global__ void __launch_bounds__(kEncThreads)
 
 cudaError_t launch_store_build_f8(const uint16_t *K, const uint16_t *V, int32_t heads, int64_t seq, int64_t v_stride,
                                   uint8_t *k_codes, uint8_t *v_codes_t, float *k_scales, float *v_scales,
-                                  float *k_mean, cudaStream_t stream) {
+                                  float *k_mean, uint32_t *err, uint64_t timeout_ns, cudaStream_t stream) {
   if (heads <= 0 || seq <= 0) return cudaSuccess;
-  f8store::stats_kernel<<<dim3(f8store::kStatCtas, static_cast<unsigned>(heads)), f8store::kStatThreads, 0,
-                          stream>>>(K, V, seq, k_mean, v_scales);
-  cudaError_t e = cudaGetLastError();
+  // statistics: one 16-CTA cluster per head (a non-portable size), else 8
+  cudaError_t e = cudaFuncSetAttribute(f8store::stats_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  for (int nc = f8store::kStatCtas; nc >= 8; nc /= 2) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(nc), static_cast<unsigned>(heads));
+    cfg.blockDim = dim3(f8store::kStatThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(nc);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (nc > 8 && (cudaOccupancyMaxActiveClusters(&clusters, f8store::stats_kernel, &cfg) != cudaSuccess ||
+                   clusters < 1)) {
+      cudaGetLastError();  // clear: fall back to the portable size
+      continue;
+    }
+    e = cudaLaunchKernelEx(&cfg, f8store::stats_kernel, K, V, seq, k_mean, v_scales);
+    break;
+  }
+  if (e != cudaSuccess) return e;
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t nblk = (seq + f8store::kBlockTok - 1) / f8store::kBlockTok;
   f8store::encode_kernel<<<dim3(static_cast<unsigned>(nblk), static_cast<unsigned>(heads)), f8store::kEncThreads, 0,
-                           stream>>>(K, V, seq, v_stride, k_mean, v_scales, k_codes, k_scales, v_codes_t);
+                           stream>>>(K, V, seq, v_stride, k_mean, v_scales, k_codes, k_scales, v_codes_t, err,
+                                     timeout_ns);
   return cudaGetLastError();
 }
 
