@@ -25,8 +25,6 @@ namespace f8store {
 
 constexpr int kStatCtas = 16;     // one cluster of CTAs per head (8 where 16 cannot launch)
 constexpr int kStatThreads = 512;
-constexpr int kStatUnroll = 4;    // row pairs per warp in flight
-constexpr int kStatWarps = kStatThreads / 32;
 constexpr int kBlockTok = 64;     // tokens per K scale block
 constexpr int kEncThreads = 128;  // 4 warps x 16 tokens = one block
 constexpr float kE4m3Max = 448.0f;
@@ -38,100 +36,141 @@ __device__ __forceinline__ void bf16x4(const uint2 w, float (&x)[4]) {
   x[3] = bf16hi_to_f32(w.y);
 }
 
-// Pass 1, grid (cluster size, heads), one cluster per head.  CTA r of n sums
-// the tokens [r * per, (r + 1) * per), per = ceil(seq / n).  Each warp reads two rows per load
-// (half-warp = row, lane = 8 channels, 16-byte loads), kStatUnroll pairs at
-// a time, stepping over the range by the CTA's warps.  Partials are combined
-// half-warp, warp, then CTA by CTA through distributed shared memory, always
-// in index order, so the result does not depend on timing.
+constexpr int kStatChunk = 64;    // rows per bulk copy
+constexpr int kStatStages = 3;    // copies in flight per CTA
+
+struct StatSmem {
+  uint8_t k[kStatStages][kStatChunk * 256];  // bf16 rows of K
+  uint8_t v[kStatStages][kStatChunk * 256];  // and of V
+  float cta_sum[128];
+  float cta_max[128];
+  uint64_t full[kStatStages];
+  int abort;
+};
+constexpr size_t kStatSmemBytes = sizeof(StatSmem) + 128;
+static_assert(kStatChunk * 256 >= (kStatThreads / 16) * 128 * 4, "partials reuse a stage buffer");
+
+// Pass 1, grid (cluster size, heads), one cluster per head.  CTA r of n
+// covers the tokens [r * per, (r + 1) * per), per = ceil(seq / n), in chunks
+// of 64 rows that bulk copies bring into a 3-stage shared-memory ring.
+// Thread t sums channels 8 (t mod 16) .. +7 of rows t/16 and t/16 + 32 of
+// every chunk.  Partials are then combined over the row groups, then CTA by
+// CTA through distributed shared memory, always in index order, so the
+// result does not depend on timing.
 __global__ void __launch_bounds__(kStatThreads)
-    stats_kernel(const uint16_t *K, const uint16_t *V, int64_t seq, float *k_mean, float *v_scales) {
-  __shared__ float part_sum[kStatWarps][128];
-  __shared__ float part_max[kStatWarps][128];
-  __shared__ float cta_sum[128];
-  __shared__ float cta_max[128];
+    stats_kernel(const uint16_t *K, const uint16_t *V, int64_t seq, float *k_mean, float *v_scales, uint32_t *err,
+                 uint64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  StatSmem &sm = *reinterpret_cast<StatSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
   const int nc = static_cast<int>(cluster.num_blocks());
   const int h = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int half = lane >> 4, l16 = lane & 15;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int g = t & 15, rg = t >> 4;
   const int64_t per = (seq + nc - 1) / nc;
   const int64_t r0 = rank * per;
   const int64_t r1 = r0 + per < seq ? r0 + per : seq;
-  const uint16_t *kh = K + static_cast<int64_t>(h) * seq * 128 + 8 * l16;
-  const uint16_t *vh = V + static_cast<int64_t>(h) * seq * 128 + 8 * l16;
+  const int n_chunks = r1 > r0 ? static_cast<int>((r1 - r0 + kStatChunk - 1) / kStatChunk) : 0;
+  const int64_t hrow = static_cast<int64_t>(h) * seq;
+
+  if (t == 0) {
+    for (int st = 0; st < kStatStages; ++st) mbar_init(smem_u32(&sm.full[st]), 1);
+    sm.abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  auto issue = [&](int c) {
+    const int st = c % kStatStages;
+    const int64_t row = r0 + static_cast<int64_t>(c) * kStatChunk;
+    const uint32_t bytes = static_cast<uint32_t>((r1 - row < kStatChunk ? r1 - row : kStatChunk) * 256);
+    const uint32_t bar = smem_u32(&sm.full[st]);
+    mbar_arrive_expect_tx(bar, 2 * bytes);
+    bulk_g2s(smem_u32(sm.k[st]), K + (hrow + row) * 128, bytes, bar);
+    bulk_g2s(smem_u32(sm.v[st]), V + (hrow + row) * 128, bytes, bar);
+  };
+  int issued = 0;
+  if (t == 0)
+    for (; issued < kStatStages && issued < n_chunks; ++issued) issue(issued);
+
+  const WaitCtx wctx{err, &sm.abort, timeout_ns};
   float s[8], m[8];
 #pragma unroll
   for (int c = 0; c < 8; ++c) s[c] = m[c] = 0.f;
-  constexpr int64_t kStep = 2 * kStatWarps;  // rows per sweep of the CTA
-  for (int64_t base = r0 + 2 * warp + half; base < r1; base += kStep * kStatUnroll) {
-    uint4 kw[kStatUnroll], vw[kStatUnroll];
+  int c = 0;
+  bool ok = true;
+  for (; c < n_chunks; ++c) {
+    const int st = c % kStatStages;
+    ok = __syncthreads_and(mbar_wait(smem_u32(&sm.full[st]), (c / kStatStages) & 1, wctx));
+    if (!ok) break;
+    const int64_t row = r0 + static_cast<int64_t>(c) * kStatChunk;
+    const int valid = static_cast<int>(r1 - row < kStatChunk ? r1 - row : kStatChunk);
 #pragma unroll
-    for (int u = 0; u < kStatUnroll; ++u) {
-      const int64_t r = base + u * kStep;
-      kw[u] = r < r1 ? *reinterpret_cast<const uint4 *>(kh + r * 128) : make_uint4(0u, 0u, 0u, 0u);
-      vw[u] = r < r1 ? *reinterpret_cast<const uint4 *>(vh + r * 128) : make_uint4(0u, 0u, 0u, 0u);
-    }
+    for (int hr = 0; hr < 2; ++hr) {
+      const int lr = rg + 32 * hr;
+      if (lr < valid) {
+        const uint4 kw = *reinterpret_cast<const uint4 *>(sm.k[st] + lr * 256 + g * 16);
+        const uint4 vw = *reinterpret_cast<const uint4 *>(sm.v[st] + lr * 256 + g * 16);
+        const uint32_t kk[4] = {kw.x, kw.y, kw.z, kw.w};
+        const uint32_t vv[4] = {vw.x, vw.y, vw.z, vw.w};
 #pragma unroll
-    for (int u = 0; u < kStatUnroll; ++u) {
-      const uint32_t kk[4] = {kw[u].x, kw[u].y, kw[u].z, kw[u].w};
-      const uint32_t vv[4] = {vw[u].x, vw[u].y, vw[u].z, vw[u].w};
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        s[2 * p] += bf16lo_to_f32(kk[p]);
-        s[2 * p + 1] += bf16hi_to_f32(kk[p]);
-        m[2 * p] = fmaxf(m[2 * p], fabsf(bf16lo_to_f32(vv[p])));
-        m[2 * p + 1] = fmaxf(m[2 * p + 1], fabsf(bf16hi_to_f32(vv[p])));
+        for (int p = 0; p < 4; ++p) {
+          s[2 * p] += bf16lo_to_f32(kk[p]);
+          s[2 * p + 1] += bf16hi_to_f32(kk[p]);
+          m[2 * p] = fmaxf(m[2 * p], fabsf(bf16lo_to_f32(vv[p])));
+          m[2 * p + 1] = fmaxf(m[2 * p + 1], fabsf(bf16hi_to_f32(vv[p])));
+        }
       }
     }
+    __syncthreads();  // the stage is free again
+    if (t == 0 && issued < n_chunks) issue(issued++);
   }
-  // the two half-warps hold the same channels: add the upper into the lower
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const float os = __shfl_down_sync(0xffffffffu, s[c], 16);
-    const float om = __shfl_down_sync(0xffffffffu, m[c], 16);
-    s[c] += os;
-    m[c] = fmaxf(m[c], om);
+  if (!ok) {
+    // copies still in flight must land before the CTA exits
+    if (t == 0)
+      for (int k = c; k < issued; ++k)
+        mbar_wait_drain(smem_u32(&sm.full[k % kStatStages]), (k / kStatStages) & 1, kDrainNs);
+    __syncthreads();
   }
-  if (half == 0) {
+  // row-group partials over the (now idle) first stage, summed in order
+  float *part_sum = reinterpret_cast<float *>(sm.k[0]);
+  float *part_max = reinterpret_cast<float *>(sm.v[0]);
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      part_sum[warp][8 * l16 + c] = s[c];
-      part_max[warp][8 * l16 + c] = m[c];
-    }
+  for (int cc = 0; cc < 8; ++cc) {
+    part_sum[rg * 128 + 8 * g + cc] = s[cc];
+    part_max[rg * 128 + 8 * g + cc] = m[cc];
   }
   __syncthreads();
-  if (threadIdx.x < 128) {
+  if (t < 128) {
     float a = 0.f, b = 0.f;
-    for (int w = 0; w < kStatWarps; ++w) {
-      a += part_sum[w][threadIdx.x];
-      b = fmaxf(b, part_max[w][threadIdx.x]);
+    for (int r = 0; r < kStatThreads / 16; ++r) {
+      a += part_sum[r * 128 + t];
+      b = fmaxf(b, part_max[r * 128 + t]);
     }
-    cta_sum[threadIdx.x] = a;
-    cta_max[threadIdx.x] = b;
+    sm.cta_sum[t] = a;
+    sm.cta_max[t] = b;
   }
   cluster.sync();
   if (rank == 0 && warp == 0) {
     float x[4] = {0.f, 0.f, 0.f, 0.f}, mx[4] = {0.f, 0.f, 0.f, 0.f};
     for (int q = 0; q < nc; ++q) {
-      const float *ps = cluster.map_shared_rank(cta_sum, q);
-      const float *pm = cluster.map_shared_rank(cta_max, q);
+      const float *ps = cluster.map_shared_rank(sm.cta_sum, q);
+      const float *pm = cluster.map_shared_rank(sm.cta_max, q);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        x[c] += ps[4 * lane + c];
-        mx[c] = fmaxf(mx[c], pm[4 * lane + c]);
+      for (int cc = 0; cc < 4; ++cc) {
+        x[cc] += ps[4 * lane + cc];
+        mx[cc] = fmaxf(mx[cc], pm[4 * lane + cc]);
       }
     }
     // mean of the raw channels, then rotated: mean(k) H = mean(k H)
     const float n = static_cast<float>(seq);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) x[c] = __fdiv_rn(x[c], n);
+    for (int cc = 0; cc < 4; ++cc) x[cc] = __fdiv_rn(x[cc], n);
     fwht128_warp(x, lane);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      k_mean[static_cast<int64_t>(h) * 128 + 4 * lane + c] = x[c] * kInvSqrt128;
-      v_scales[static_cast<int64_t>(h) * 128 + 4 * lane + c] = __fdiv_rn(mx[c], kE4m3Max);
+    for (int cc = 0; cc < 4; ++cc) {
+      k_mean[static_cast<int64_t>(h) * 128 + 4 * lane + cc] = x[cc] * kInvSqrt128;
+      v_scales[static_cast<int64_t>(h) * 128 + 4 * lane + cc] = __fdiv_rn(mx[cc], kE4m3Max);
     }
   }
   // the peers' shared memory must outlive rank 0's reads
@@ -281,10 +320,14 @@ cudaError_t launch_store_build_f8(const uint16_t *K, const uint16_t *V, int32_t 
   // statistics: one 16-CTA cluster per head (a non-portable size), else 8
   cudaError_t e = cudaFuncSetAttribute(f8store::stats_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(f8store::stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(f8store::kStatSmemBytes));
+  if (e != cudaSuccess) return e;
   for (int nc = f8store::kStatCtas; nc >= 8; nc /= 2) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(nc), static_cast<unsigned>(heads));
     cfg.blockDim = dim3(f8store::kStatThreads);
+    cfg.dynamicSmemBytes = f8store::kStatSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -299,7 +342,7 @@ cudaError_t launch_store_build_f8(const uint16_t *K, const uint16_t *V, int32_t 
       cudaGetLastError();  // clear: fall back to the portable size
       continue;
     }
-    e = cudaLaunchKernelEx(&cfg, f8store::stats_kernel, K, V, seq, k_mean, v_scales);
+    e = cudaLaunchKernelEx(&cfg, f8store::stats_kernel, K, V, seq, k_mean, v_scales, err, timeout_ns);
     break;
   }
   if (e != cudaSuccess) return e;
