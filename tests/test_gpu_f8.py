@@ -257,3 +257,37 @@ def test_f8_full_size_h32_l217088(cuda):
     rows = torch.linspace(0, w["seq"] - 1, 64).long()
     compare_f8_attention(out[heads][:, rows], q[heads][:, rows].cpu(), gpu_store_numpy(st, heads),
                          "h32 l217088 sampled")
+
+
+@pytest.mark.parametrize("softmax_scale", [0.02, 0.3])
+def test_attend_f8_softmax_scale(cuda, softmax_scale):
+    # a flatter and a sharper softmax than the default 1/sqrt(128)
+    b = _b()
+    q, k, v = synth.make_qkv(2, 1500, seed=21, k_outliers=True)
+    st = _build(k.to(cuda), v.to(cuda))
+    out = b.attend_f8(q.to(cuda), st, q_chunk=512, kv_block=512, softmax_scale=softmax_scale)
+    b.sync_status()
+    store = gpu_store_numpy(st)
+    ref = f8.attend_kvf8s(q, store, scale=softmax_scale)
+    B = error_bound(q, store, scale=softmax_scale)
+    err = np.abs(out.cpu().double().numpy() - ref)
+    assert np.all(err <= B + SLACK) and err.mean() <= 0.25 * B.mean()
+
+
+def test_attend_f8_query_outliers_and_zero_keys(cuda):
+    # query rows 100x larger than the rest (their own fp32 scale), and a
+    # second head whose keys are all zero (every score 0: the mean of V)
+    b = _b()
+    q, k, v = synth.make_qkv(2, 900, seed=22)
+    q = q.float()
+    q[:, ::7] *= 100
+    q = q.to(torch.bfloat16)
+    k = k.clone()
+    k[1] = 0
+    st = _build(k.to(cuda), v.to(cuda))
+    out = b.attend_f8(q.to(cuda), st, q_chunk=300, kv_block=256)
+    b.sync_status()
+    store = gpu_store_numpy(st)
+    compare_f8_attention(out, q, store, "q outliers / zero keys")
+    mean_v = f8.dequant_v(store, 1).mean(axis=0)
+    assert np.max(np.abs(out[1].cpu().double().numpy() - mean_v[None, :])) < 1e-5

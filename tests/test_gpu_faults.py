@@ -41,13 +41,14 @@ def test_selftest_wait_runs_out_and_context_survives(cuda):
     _tiny_check(cuda)
 
 
-@pytest.mark.parametrize("path", ["store", "kvi8r", "exact"])
+@pytest.mark.parametrize("path", ["store", "kvi8r", "exact", "store_f8", "kvf8s"])
 def test_kernels_give_up_under_tiny_wait_limit(cuda, path):
     b = _b()
     s = torch.cuda.current_stream().cuda_stream
     q, k, v = synth.make_qkv(2, 4096, seed=3)
     q, k, v = q.to(cuda), k.to(cuda), v.to(cuda)
     st = b.build_store(k, v)
+    st8 = b.build_store_f8(k, v)
     assert b.h3kv_sync_status(s) == b.H3KV_OK
     b.check(b.h3kv_set_wait_timeout_ns(1))
     try:
@@ -55,15 +56,20 @@ def test_kernels_give_up_under_tiny_wait_limit(cuda, path):
             b.build_store(k, v, out=st)
         elif path == "kvi8r":
             b.attend(q, st, q_chunk=4096, kv_block=0)
-        else:
+        elif path == "exact":
             b.attend_exact(q, k, v, q_chunk=4096, kv_block=0)
+        elif path == "store_f8":
+            b.build_store_f8(k, v, out=st8)
+        else:
+            b.attend_f8(q, st8, q_chunk=4096, kv_block=0)
         status = b.h3kv_sync_status(s)
     finally:
         b.check(b.h3kv_set_wait_timeout_ns(0))
-    if path == "store":
-        # the store build's waits (TMA landing in shared memory) usually end
-        # inside the first suspended try_wait, before the limit is checked;
-        # either outcome is fine as long as the call ends and the word clears
+    if path in ("store", "store_f8"):
+        # the store builds' waits (bulk copies landing in shared memory)
+        # usually end inside the first suspended try_wait, before the limit is
+        # checked; either outcome is fine as long as the call ends and the
+        # word clears
         assert status in (b.H3KV_OK, b.H3KV_ERR_DEVICE_TIMEOUT)
     else:
         assert status == b.H3KV_ERR_DEVICE_TIMEOUT
