@@ -237,7 +237,8 @@ h3kv_status h3kv_attend(const uint16_t *Q, int64_t q_seq, const h3kv_store *stor
   for (int64_t c0 = 0; c0 < q_seq; c0 += q_chunk) {
     a.q_begin = c0;
     a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
-    if (h3kv::launch_attend_kvi8r(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return H3KV_ERR_CUDA;
+    if (h3kv::launch_attend_kvi8r(a, c0 > 0, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return H3KV_ERR_CUDA;
   }
   return H3KV_OK;
 }
@@ -279,7 +280,7 @@ h3kv_status h3kv_attend_exact(const uint16_t *Q, int64_t q_seq, const uint16_t *
   for (int64_t c0 = 0; c0 < q_seq; c0 += q_chunk) {
     a.q_begin = c0;
     a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
-    if (h3kv::launch_attend_exact(tq, tk, tv, a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (h3kv::launch_attend_exact(tq, tk, tv, a, c0 > 0, static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return H3KV_ERR_CUDA;
   }
   return H3KV_OK;
@@ -355,7 +356,8 @@ h3kv_status h3kv_attend_staged(const uint16_t *Q, int64_t q_seq, const h3kv_stor
     for (int64_t c0 = 0; c0 < q_seq; c0 += q_chunk) {
       a.q_begin = c0;
       a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
-      if (h3kv::launch_attend_kvi8r(a, s) != cudaSuccess) return H3KV_ERR_CUDA;
+      // staged launches carry state from block to block: never overlapped
+      if (h3kv::launch_attend_kvi8r(a, false, s) != cudaSuccess) return H3KV_ERR_CUDA;
     }
   }
   return H3KV_OK;
@@ -434,7 +436,8 @@ h3kv_status h3kv_attend_f8(const uint16_t *Q, int64_t q_seq, const h3kv_store_f8
   for (int64_t c0 = 0; c0 < q_seq; c0 += q_chunk) {
     a.q_begin = c0;
     a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
-    if (h3kv::launch_attend_f8(tk, tv, a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return H3KV_ERR_CUDA;
+    if (h3kv::launch_attend_f8(tk, tv, a, c0 > 0, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return H3KV_ERR_CUDA;
   }
   return H3KV_OK;
 }

@@ -209,6 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the next query chunk's launch may fill SMs that this grid's tail frees
+  if (tid == 0) pdl_launch_dependents();
   const uint32_t tmem = sm.tmem_base;
   const WaitCtx wctx{a.err, &sm.abort, a.timeout_ns};
 
@@ -631,6 +633,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // complete only after the launch this one overlapped
+  if (tid == 0) pdl_wait_prerequisites();
 }
 
 }  // namespace attn

@@ -4,7 +4,7 @@
 namespace h3kv {
 
 cudaError_t launch_attend_exact(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                                const AttnArgs &args, cudaStream_t stream) {
+                                const AttnArgs &args, bool overlap_previous, cudaStream_t stream) {
   const int64_t rows = args.q_end - args.q_begin;
   if (rows <= 0 || args.heads <= 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(attn::attend_kernel<false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -12,8 +12,8 @@ cudaError_t launch_attend_exact(const CUtensorMap &q, const CUtensorMap &k, cons
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>((rows + kAttnRowsPerCta - 1) / kAttnRowsPerCta),
                   static_cast<unsigned>(args.heads));
-  attn::attend_kernel<false, 1><<<grid, attn::kThreads, attn::kSmemBytes, stream>>>(q, k, v, args);
-  return cudaGetLastError();
+  return launch_maybe_overlapped(attn::attend_kernel<false, 1>, grid, attn::kSmemBytes, overlap_previous, stream, q,
+                                 k, v, args);
 }
 
 }  // namespace h3kv

@@ -98,6 +98,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the next query chunk's launch may fill SMs that this grid's tail frees
+  if (tid == 0) pdl_launch_dependents();
   const uint32_t tmem = sm.tmem_base;
   const WaitCtx wctx{a.err, &sm.abort, a.timeout_ns};
 
@@ -443,6 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // complete only after the launch this one overlapped
+  if (tid == 0) pdl_wait_prerequisites();
 }
 
 }  // namespace attn_f8
@@ -450,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 size_t attend_f8_smem_bytes() { return attn_f8::kSmemBytes; }
 
 cudaError_t launch_attend_f8(const CUtensorMap &k_codes, const CUtensorMap &v_codes_t, const F8Args &args,
-                             cudaStream_t stream) {
+                             bool overlap_previous, cudaStream_t stream) {
   const int64_t rows = args.q_end - args.q_begin;
   if (rows <= 0 || args.heads <= 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(attn_f8::attend_f8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -458,8 +462,8 @@ cudaError_t launch_attend_f8(const CUtensorMap &k_codes, const CUtensorMap &v_co
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>((rows + kAttnRowsPerCta - 1) / kAttnRowsPerCta),
                   static_cast<unsigned>(args.heads));
-  attn_f8::attend_f8_kernel<<<grid, attn::kThreads, attn_f8::kSmemBytes, stream>>>(k_codes, v_codes_t, args);
-  return cudaGetLastError();
+  return launch_maybe_overlapped(attn_f8::attend_f8_kernel, grid, attn_f8::kSmemBytes, overlap_previous, stream,
+                                 k_codes, v_codes_t, args);
 }
 
 }  // namespace h3kv

@@ -5,7 +5,7 @@ namespace h3kv {
 
 size_t attend_smem_bytes() { return attn::kSmemBytes; }
 
-cudaError_t launch_attend_kvi8r(const AttnArgs &args, cudaStream_t stream) {
+cudaError_t launch_attend_kvi8r(const AttnArgs &args, bool overlap_previous, cudaStream_t stream) {
   const int64_t rows = args.q_end - args.q_begin;
   if (rows <= 0 || args.heads <= 0) return cudaSuccess;
   // one scale per row, or one per 32 values
@@ -17,8 +17,8 @@ cudaError_t launch_attend_kvi8r(const AttnArgs &args, cudaStream_t stream) {
   memset(&unused, 0, sizeof(unused));
   const dim3 grid(static_cast<unsigned>((rows + kAttnRowsPerCta - 1) / kAttnRowsPerCta),
                   static_cast<unsigned>(args.heads));
-  kernel<<<grid, attn::kThreads, attn::kSmemBytes, stream>>>(unused, unused, unused, args);
-  return cudaGetLastError();
+  return launch_maybe_overlapped(kernel, grid, attn::kSmemBytes, overlap_previous, stream, unused, unused, unused,
+                                 args);
 }
 
 }  // namespace h3kv

@@ -8,6 +8,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace h3kv {
 
 // Store build over `rows` = heads * seq rows of K and V.  Tensor maps: bf16
@@ -51,7 +53,11 @@ constexpr int kAttnRowsPerCta = 256;  // two 128-row query tiles per CTA
 // The exact path reads Q, K, V through 3-D tensor maps ({128, seq, heads},
 // box 64 x 128 x 1, 128B swizzle); the kvi8r path reads Q with plain loads
 // and the store with bulk copies (the maps are unused).
-cudaError_t launch_attend_kvi8r(const AttnArgs &args, cudaStream_t stream);
+// overlap_previous: launch with programmatic stream serialization, so that
+// this grid's CTAs may start on SMs the previous launch's tail frees.  Only
+// for a launch that touches nothing the previous kernel writes (the next
+// query chunk of the same call); the kernels keep completion in stream order.
+cudaError_t launch_attend_kvi8r(const AttnArgs &args, bool overlap_previous, cudaStream_t stream);
 
 // kvf8s store build: statistics pass (K mean, V channel absmax) then the
 // encode pass.  V codes are written channel-major with row stride v_stride
@@ -81,10 +87,28 @@ struct F8Args {
 // seq, heads} and channel-major V codes through {seq, 128, heads}, both u8,
 // box 128 x 128 x 1, 128B swizzle.
 cudaError_t launch_attend_f8(const CUtensorMap &k_codes, const CUtensorMap &v_codes_t, const F8Args &args,
-                             cudaStream_t stream);
+                             bool overlap_previous, cudaStream_t stream);
 size_t attend_f8_smem_bytes();
 cudaError_t launch_attend_exact(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                                const AttnArgs &args, cudaStream_t stream);
+                                const AttnArgs &args, bool overlap_previous, cudaStream_t stream);
 size_t attend_smem_bytes();
+
+// Launch `kernel` (512 threads) normally, or with programmatic stream
+// serialization when `overlap` is set.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_maybe_overlapped(void (*kernel)(KArgs...), dim3 grid, size_t smem, bool overlap,
+                                    cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(512);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace h3kv

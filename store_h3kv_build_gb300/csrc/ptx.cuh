@@ -281,6 +281,17 @@ __device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
+// Programmatic dependent launch.  Let the next kernel of the stream, when it
+// is launched with programmatic stream serialization, start its CTAs once
+// every CTA of this grid has executed this (or exited).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Block until the grids this one was allowed to overlap have completed (an
+// immediate return for a normal launch).  Called at a kernel's end, it keeps
+// completion in stream order.
+__device__ __forceinline__ void pdl_wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Arrive once on `bar` when every prior tcgen05 async op of this thread is done.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
