@@ -74,9 +74,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity.  Returns false (after
-// recording the timeout) if the limit ran out or another role aborted.
+// recording the timeout) if the limit ran out or another role aborted.  A
+// phase that is already complete costs one poll: the global timer (a slow
+// read) is only consulted once a poll has failed, and the limit counts from
+// there.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx &w) {
-  // the limit counts from the start of the wait (one timer read up front)
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (*w.abort) return false;
@@ -91,6 +94,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 
 // Bounded wait used while draining after an abort: ignores the abort flag.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer_ns() - t0 > timeout_ns) return false;
