@@ -148,6 +148,29 @@ h3kv_status h3kv_attend_staged(const uint16_t *Q, int64_t q_seq, const h3kv_stor
                                int32_t kv_block, float softmax_scale, float *O, void *staging,
                                size_t staging_bytes, float *state, void *stream);
 
+/* Device scratch bytes h3kv_attend_hostio needs: two query chunks of Q
+ * (bf16) and two of O (fp32) for every head, 2 * heads * q_chunk * 128 * 6.
+ * Returns 0 for invalid arguments. */
+size_t h3kv_hostio_scratch_bytes(int32_t heads, int32_t q_chunk);
+
+/* h3kv_attend with Q and O in host memory (pinned for asynchronous copies),
+ * streamed through HBM one query chunk at a time -- the q_chunk input's way
+ * of bounding the device transient.  The rows of chunk c are copied in, attended over
+ * the (device-resident) store, and copied back.  The copies of other chunks
+ * run on a second stream that the library creates for the call, so they
+ * overlap the attention of chunk c.  The result is bit-identical to
+ * h3kv_attend with device Q and O and the same q_chunk and kv_block.
+ *   Q_host: bf16 [store->heads, q_seq, 128]; O_host: fp32, same shape.
+ *   scratch: device memory >= h3kv_hostio_scratch_bytes(store->heads,
+ *   q_chunk), 16-byte aligned, caller-owned, reused by each call (calls that
+ *   overlap on the GPU must not share it).
+ * All work, copies included, is ordered after earlier work on `stream`, and
+ * later work on `stream` sees O_host written.  Other arguments and errors as
+ * h3kv_attend. */
+h3kv_status h3kv_attend_hostio(const uint16_t *Q_host, int64_t q_seq, const h3kv_store *store, int32_t q_chunk,
+                               int32_t kv_block, float softmax_scale, float *O_host, void *scratch,
+                               size_t scratch_bytes, void *stream);
+
 /* Size of the fixed device scratch that h3kv_attend_staged_static uses. */
 #define H3KV_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
 

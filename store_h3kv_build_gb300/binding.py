@@ -68,6 +68,9 @@ _SIGS = {
                                                  _vp]),
     "h3kv_attend_staged": (ctypes.c_int, [_vp, _i64, ctypes.POINTER(h3kv_store), _i32, _i32, _f32, _vp, _vp,
                                           ctypes.c_size_t, _vp, _vp]),
+    "h3kv_hostio_scratch_bytes": (ctypes.c_size_t, [_i32, _i32]),
+    "h3kv_attend_hostio": (ctypes.c_int, [_vp, _i64, ctypes.POINTER(h3kv_store), _i32, _i32, _f32, _vp, _vp,
+                                          ctypes.c_size_t, _vp]),
     "h3kv_f8_v_stride": (ctypes.c_int64, [_i64]),
     "h3kv_store_f8_bytes": (ctypes.c_size_t, [_i32, _i64, _i32]),
     "h3kv_build_store_f8": (ctypes.c_int, [_vp, _vp, _i32, _i64, _i32, ctypes.POINTER(h3kv_store_f8), _vp]),
@@ -189,6 +192,28 @@ def attend_staged(Q: torch.Tensor, store: Store, q_chunk: int = 16384, kv_block:
     check(h3kv_attend_staged(_ptr(Q), q_seq, ctypes.byref(st), int(q_chunk), int(kv_block), float(softmax_scale),
                              _ptr(out), _ptr(staging), staging.numel() * staging.element_size(), _ptr(state),
                              _stream(stream)), "h3kv_attend_staged")
+    return out
+
+
+def attend_hostio(Q_host: torch.Tensor, store: Store, q_chunk: int = 16384, kv_block: int = 0,
+                  softmax_scale: float = 0.0, out: torch.Tensor | None = None, scratch: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """h3kv_attend_hostio: kvi8r attention of bf16 Q in (pinned) host memory
+    over a device store, streamed through HBM per query chunk; the fp32
+    output lands in host memory (``out``, pinned, created here if not
+    given).  ``scratch`` (uint8 device, >= h3kv_hostio_scratch_bytes) is
+    created here if not given."""
+    heads, q_seq = int(Q_host.shape[0]), int(Q_host.shape[1])
+    if out is None:
+        out = torch.empty(Q_host.shape, dtype=torch.float32, pin_memory=True)
+    if scratch is None:
+        dev = store.k_codes.device
+        scratch = torch.empty(max(int(h3kv_hostio_scratch_bytes(heads, int(q_chunk))), 16), dtype=torch.uint8,
+                              device=dev)
+    st = store.c_struct()
+    check(h3kv_attend_hostio(_ptr(Q_host), q_seq, ctypes.byref(st), int(q_chunk), int(kv_block),
+                             float(softmax_scale), _ptr(out), _ptr(scratch), scratch.numel(), _stream(stream)),
+          "h3kv_attend_hostio")
     return out
 
 

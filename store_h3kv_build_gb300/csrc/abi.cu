@@ -363,6 +363,110 @@ h3kv_status h3kv_attend_staged(const uint16_t *Q, int64_t q_seq, const h3kv_stor
   return H3KV_OK;
 }
 
+size_t h3kv_hostio_scratch_bytes(int32_t heads, int32_t q_chunk) {
+  if (heads < 0 || q_chunk < 1) return 0;
+  return 2 * static_cast<size_t>(heads) * static_cast<size_t>(q_chunk) * H3KV_HEAD_DIM * (2 + 4);
+}
+
+h3kv_status h3kv_attend_hostio(const uint16_t *Q_host, int64_t q_seq, const h3kv_store *store, int32_t q_chunk,
+                               int32_t kv_block, float softmax_scale, float *O_host, void *scratch,
+                               size_t scratch_bytes, void *stream) {
+  if (!store || q_seq < 0 || store->heads < 0 || store->seq < 0) return H3KV_ERR_INVALID_ARG;
+  if (store->head_dim != H3KV_HEAD_DIM) return H3KV_ERR_UNSUPPORTED;
+  h3kv_status st = check_chunks(q_chunk, kv_block);
+  if (st != H3KV_OK) return st;
+  const int groups = scale_groups_of(store);
+  if (groups == 0) return H3KV_ERR_INVALID_ARG;
+  if (store->heads == 0 || q_seq == 0) return H3KV_OK;
+  if (store->seq == 0) return H3KV_ERR_INVALID_ARG;
+  const int64_t H = store->heads;
+  if (H * q_seq > kMaxRows || H * store->seq > kMaxRows) return H3KV_ERR_INVALID_ARG;
+  if (!Q_host || !O_host || !scratch || !store->k_codes || !store->v_codes || !store->k_scales ||
+      !store->v_scales)
+    return H3KV_ERR_INVALID_ARG;
+  if (!aligned16(scratch) || !aligned16(store->k_codes) || !aligned16(store->v_codes) ||
+      !aligned16(store->k_scales) || !aligned16(store->v_scales))
+    return H3KV_ERR_INVALID_ARG;
+  if (scratch_bytes < h3kv_hostio_scratch_bytes(store->heads, q_chunk)) return H3KV_ERR_INVALID_ARG;
+  DeviceInfo *d = nullptr;
+  st = device_info(&d);
+  if (st != H3KV_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // scratch: Q chunks [2][H, q_chunk, 128] bf16, then O chunks [2][H, q_chunk, 128] fp32
+  const int64_t qc = q_chunk;
+  uint16_t *qbuf[2];
+  float *obuf[2];
+  qbuf[0] = static_cast<uint16_t *>(scratch);
+  qbuf[1] = qbuf[0] + H * qc * 128;
+  obuf[0] = reinterpret_cast<float *>(qbuf[1] + H * qc * 128);
+  obuf[1] = obuf[0] + H * qc * 128;
+  const int32_t kvb = kv_block == 0 ? H3KV_DEFAULT_KV_BLOCK : kv_block;
+  h3kv::AttnArgs a{};
+  a.k_codes = store->k_codes;
+  a.v_codes = store->v_codes;
+  a.k_scales = store->k_scales;
+  a.v_scales = store->v_scales;
+  a.q_seq = qc;  // row stride of a chunk buffer
+  a.kv_seq = store->seq;
+  a.kv_stride = store->seq;
+  a.scale_groups = groups;
+  a.heads = store->heads;
+  a.kv_block_tiles = kvb / H3KV_KV_TILE;
+  a.scale_log2 = scale_log2_of(softmax_scale);
+  a.err = d->err;
+  a.timeout_ns = g_timeout_ns.load();
+  a.q_begin = 0;
+
+  // the copy stream and the events live for this call only (destroying them
+  // with work pending is allowed: they are released once it completes)
+  cudaStream_t cs = nullptr;
+  cudaEvent_t entry = nullptr, fin = nullptr, q_ready[2] = {nullptr, nullptr}, att_done[2] = {nullptr, nullptr};
+  h3kv_status result = H3KV_OK;
+  auto fail = [&](cudaError_t e) {
+    if (e != cudaSuccess && result == H3KV_OK) result = H3KV_ERR_CUDA;
+    return e != cudaSuccess;
+  };
+  const unsigned ef = cudaEventDisableTiming;
+  if (!fail(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking)) && !fail(cudaEventCreateWithFlags(&entry, ef)) &&
+      !fail(cudaEventCreateWithFlags(&fin, ef)) && !fail(cudaEventCreateWithFlags(&q_ready[0], ef)) &&
+      !fail(cudaEventCreateWithFlags(&q_ready[1], ef)) && !fail(cudaEventCreateWithFlags(&att_done[0], ef)) &&
+      !fail(cudaEventCreateWithFlags(&att_done[1], ef))) {
+    const int64_t n = (q_seq + qc - 1) / qc;
+    auto rows_of = [&](int64_t c) { return (c + 1) * qc <= q_seq ? qc : q_seq - c * qc; };
+    // Q rows [c qc, c qc + rows) of every head -> chunk buffer b
+    auto copy_in = [&](int64_t c, int b) {
+      return cudaMemcpy2DAsync(qbuf[b], qc * 256, Q_host + c * qc * 128, q_seq * 256, rows_of(c) * 256, H,
+                               cudaMemcpyHostToDevice, cs);
+    };
+    auto copy_out = [&](int64_t c, int b) {
+      return cudaMemcpy2DAsync(O_host + c * qc * 128, q_seq * 512, obuf[b], qc * 512, rows_of(c) * 512, H,
+                               cudaMemcpyDeviceToHost, cs);
+    };
+    // the copies start after everything queued on the caller's stream
+    bool ok = !fail(cudaEventRecord(entry, s)) && !fail(cudaStreamWaitEvent(cs, entry, 0));
+    for (int64_t c = 0; ok && c < 2 && c < n; ++c)
+      ok = !fail(copy_in(c, static_cast<int>(c))) && !fail(cudaEventRecord(q_ready[c], cs));
+    for (int64_t c = 0; ok && c < n; ++c) {
+      const int b = static_cast<int>(c & 1);
+      a.q = qbuf[b];
+      a.o = obuf[b];
+      a.q_end = rows_of(c);
+      ok = !fail(cudaStreamWaitEvent(s, q_ready[b], 0)) && !fail(h3kv::launch_attend_kvi8r(a, false, s)) &&
+           !fail(cudaEventRecord(att_done[b], s)) && !fail(cudaStreamWaitEvent(cs, att_done[b], 0)) &&
+           !fail(copy_out(c, b));
+      // buffer b is free again for chunk c + 2 once its O rows are out
+      if (ok && c + 2 < n) ok = !fail(copy_in(c + 2, b)) && !fail(cudaEventRecord(q_ready[b], cs));
+    }
+    // later work on the caller's stream sees every O row in host memory
+    if (ok) ok = !fail(cudaEventRecord(fin, cs)) && !fail(cudaStreamWaitEvent(s, fin, 0));
+    (void)ok;
+  }
+  for (cudaEvent_t e : {entry, fin, q_ready[0], q_ready[1], att_done[0], att_done[1]})
+    if (e) cudaEventDestroy(e);
+  if (cs) cudaStreamDestroy(cs);
+  return result;
+}
+
 int64_t h3kv_f8_v_stride(int64_t seq) { return seq < 0 ? 0 : (seq + 15) / 16 * 16; }
 
 size_t h3kv_store_f8_bytes(int32_t heads, int64_t seq, int32_t head_dim) {

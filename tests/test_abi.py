@@ -165,3 +165,17 @@ def test_attend_f8_rejects_bad_arguments():
     assert at(4096, 256, ctypes.byref(st), 64, 0, 0.0, 0, None) == b.H3KV_ERR_INVALID_ARG        # null O
     assert at(4096, 256, ctypes.byref(_store_f8(seq=0)), 64, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
     assert at(4096, 0, ctypes.byref(st), 64, 0, 0.0, 4096, None) == b.H3KV_OK
+
+
+def test_hostio_checks():
+    assert b.h3kv_hostio_scratch_bytes(32, 16384) == 2 * 32 * 16384 * 128 * 6
+    assert b.h3kv_hostio_scratch_bytes(1, 0) == 0 and b.h3kv_hostio_scratch_bytes(-1, 10) == 0
+    st = _store()
+    hi = b.h3kv_attend_hostio
+    need = b.h3kv_hostio_scratch_bytes(1, 64)
+    assert hi(4096, 256, ctypes.byref(st), 64, 0, 0.0, 4096, 4096, need - 1, None) == b.H3KV_ERR_INVALID_ARG
+    assert hi(4096, 256, ctypes.byref(st), 64, 0, 0.0, 4096, 0, need, None) == b.H3KV_ERR_INVALID_ARG
+    assert hi(4096, 256, ctypes.byref(st), 64, 0, 0.0, 4096, 4100, need, None) == b.H3KV_ERR_INVALID_ARG
+    assert hi(0, 256, ctypes.byref(st), 64, 0, 0.0, 4096, 4096, need, None) == b.H3KV_ERR_INVALID_ARG
+    assert hi(4096, 256, ctypes.byref(st), 0, 0, 0.0, 4096, 4096, need, None) == b.H3KV_ERR_INVALID_ARG
+    assert hi(4096, 0, ctypes.byref(st), 64, 0, 0.0, 4096, 4096, need, None) == b.H3KV_OK
