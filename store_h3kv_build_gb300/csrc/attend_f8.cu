@@ -451,8 +451,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace attn_f8
 
-size_t attend_f8_smem_bytes() { return attn_f8::kSmemBytes; }
-
 cudaError_t launch_attend_f8(const CUtensorMap &k_codes, const CUtensorMap &v_codes_t, const F8Args &args,
                              bool overlap_previous, cudaStream_t stream) {
   const int64_t rows = args.q_end - args.q_begin;

@@ -3,8 +3,6 @@
 
 namespace h3kv {
 
-size_t attend_smem_bytes() { return attn::kSmemBytes; }
-
 cudaError_t launch_attend_kvi8r(const AttnArgs &args, bool overlap_previous, cudaStream_t stream) {
   const int64_t rows = args.q_end - args.q_begin;
   if (rows <= 0 || args.heads <= 0) return cudaSuccess;

@@ -19,7 +19,6 @@ cudaError_t launch_store_build(const CUtensorMap &k_in, const CUtensorMap &v_in,
                                const CUtensorMap &v_out, uint16_t *k_scales, uint16_t *v_scales, int64_t rows,
                                int num_sms, int scale_groups, uint32_t *err, uint64_t timeout_ns,
                                cudaStream_t stream);
-size_t store_build_smem_bytes();
 
 struct AttnArgs {
   const uint16_t *q;        // bf16 [heads, q_seq, 128]
@@ -88,10 +87,8 @@ struct F8Args {
 // box 128 x 128 x 1, 128B swizzle.
 cudaError_t launch_attend_f8(const CUtensorMap &k_codes, const CUtensorMap &v_codes_t, const F8Args &args,
                              bool overlap_previous, cudaStream_t stream);
-size_t attend_f8_smem_bytes();
 cudaError_t launch_attend_exact(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                                 const AttnArgs &args, bool overlap_previous, cudaStream_t stream);
-size_t attend_smem_bytes();
 
 // Launch `kernel` (512 threads) normally, or with programmatic stream
 // serialization when `overlap` is set.

@@ -357,18 +357,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
-// 32 lanes x 64 columns -> 64 registers per thread: two 32-column loads in
-// flight together, then one wait.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-      : "r"(taddr), "r"(taddr + 32)
-      : "memory");
-}
-
 // 32 lanes x 128 columns -> 128 registers per thread: four 32-column loads
 // in flight together, then one wait.
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
@@ -424,24 +412,11 @@ __device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_fl
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // In-register fast Walsh-Hadamard transform of 128 values (Sylvester order,
-// unnormalised): y_j = sum_i x_i (-1)^popcount(i & j).  7 butterfly stages.
-__device__ __forceinline__ void fwht128(float (&x)[128]) {
-#pragma unroll
-  for (int h = 1; h < 128; h <<= 1) {
-#pragma unroll
-    for (int i = 0; i < 128; ++i) {
-      if ((i & h) == 0) {
-        const float a = x[i], b = x[i + h];
-        x[i] = a + b;
-        x[i + h] = a - b;
-      }
-    }
-  }
-}
-
-// Same transform with the butterflies of strides 2 .. 64 done two at a time
-// in packed fp32 (a + b with one add, a - b as fma(b, -1, a), both exactly
-// rounded, so the result is bit-identical to the scalar version).
+// unnormalised): y_j = sum_i x_i (-1)^popcount(i & j), in 7 butterfly
+// stages.  Stride 1 runs in scalar; the butterflies of strides 2 .. 64 run
+// two at a time in packed fp32 (a + b with one add, a - b as fma(b, -1, a),
+// both exactly rounded, so every value is the scalar transform's bit for
+// bit).
 __device__ __forceinline__ void fwht128_packed(float (&x)[128]) {
 #pragma unroll
   for (int i = 0; i < 128; i += 2) {

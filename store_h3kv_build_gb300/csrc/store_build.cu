@@ -233,8 +233,6 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 }  // namespace
 
-size_t store_build_smem_bytes() { return kBuildSmemBytes; }
-
 cudaError_t launch_store_build(const CUtensorMap &k_in, const CUtensorMap &v_in, const CUtensorMap &k_out,
                                const CUtensorMap &v_out, uint16_t *k_scales, uint16_t *v_scales, int64_t rows,
                                int num_sms, int scale_groups, uint32_t *err, uint64_t timeout_ns,
