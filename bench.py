@@ -177,6 +177,26 @@ def time_oracle_sample(w, rows=512, head=0, seed=0):
     return att, gbs, t2 - t0, desc
 
 
+def time_oracle_sample_f8(w, rows=256, seed=0):
+    """The kvf8s oracle on a bounded sample: the store of one head (all
+    `seq` tokens) and `rows` query rows of that head attended over it.
+    Returns (attention TFLOP/s, store GB/s, seconds, desc)."""
+    from oracle import kvf8s as f8
+    q = synth.normal_bf16((1, rows, HEAD_DIM), seed + 100)
+    k = synth.make_k(1, w["seq"], seed + 101, w["k_outliers"])
+    v = synth.normal_bf16((1, w["seq"], HEAD_DIM), seed + 102)
+    t0 = time.perf_counter()
+    st = f8.build_store_kvf8s(k, v)
+    t1 = time.perf_counter()
+    f8.attend_kvf8s(q, st)
+    t2 = time.perf_counter()
+    att = attention_flops(1, rows, w["seq"]) / (t2 - t1) / 1e12
+    gbs = f8_store_bytes(1, w["seq"]) / (t1 - t0) / 1e9
+    desc = (f"kvf8s oracle (NumPy fp64): store of 1 head x {w['seq']} tokens, then {rows} query rows of that "
+            f"head attended over all {w['seq']} keys")
+    return att, gbs, t2 - t0, desc
+
+
 def max_over_ranks(values, device=None):
     """Element-wise max of a list of timings over all ranks (a no-op without
     an initialised process group).  Timings are the max over ranks, so the
@@ -448,6 +468,10 @@ def run_ours(args, w, name):
             att, gbs, s, desc = time_oracle_sample(w, rows=args.ref_rows)
             line["cpu_baseline"] = {"value": att, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
                                     "sample": desc, "store_gbs": gbs, "seconds": s}
+            att8, gbs8, s8, desc8 = time_oracle_sample_f8(w)
+            line["f8_store"]["cpu_baseline"] = {"value": att8, "unit": UNIT, "cores": blas_threads(),
+                                                "kind": "oracle", "sample": desc8, "store_gbs": gbs8,
+                                                "seconds": s8}
         print(json.dumps(line), flush=True)
     if dist:
         import torch.distributed as tdist
