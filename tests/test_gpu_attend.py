@@ -168,3 +168,31 @@ def test_kvi8r_close_to_exact(cuda):
     o1, _ = _kvi8r(q, k, v, 4096, 0)
     o2 = _exact(q, k, v, 4096, 0)
     assert oracle.rel_rms(o1.cpu(), o2.cpu()) < 5e-2
+
+
+def test_calls_on_one_output_stay_in_stream_order(cuda):
+    # Launches 2..n of one call overlap the previous launch's tail; the first
+    # launch of every call must still wait for everything before it.  Calls
+    # that write the same O back to back (different stores, q_chunks and
+    # paths) must leave exactly the last call's result.
+    b = _b()
+    q, k, v = synth.make_qkv(2, 3000, seed=41, k_outliers=True, device=cuda)
+    st1 = b.build_store(k, v)
+    st2 = b.build_store(v, k)
+    ref1 = b.attend(q, st1, q_chunk=3000, kv_block=1024)
+    ref2 = b.attend(q, st2, q_chunk=3000, kv_block=1024)
+    ref_x = b.attend_exact(q, k, v, q_chunk=3000, kv_block=0)
+    o = torch.empty_like(ref1)
+    for _ in range(3):
+        b.attend(q, st1, q_chunk=256, kv_block=1024, out=o)
+        b.attend(q, st2, q_chunk=700, kv_block=1024, out=o)
+    b.sync_status()
+    assert torch.equal(o, ref2)
+    b.attend(q, st2, q_chunk=300, kv_block=1024, out=o)
+    b.attend_exact(q, k, v, q_chunk=256, kv_block=0, out=o)
+    b.sync_status()
+    assert torch.equal(o, ref_x)
+    b.attend_exact(q, k, v, q_chunk=512, kv_block=0, out=o)
+    b.attend(q, st1, q_chunk=1000, kv_block=1024, out=o)
+    b.sync_status()
+    assert torch.equal(o, ref1)
