@@ -291,3 +291,19 @@ def test_attend_f8_query_outliers_and_zero_keys(cuda):
     compare_f8_attention(out, q, store, "q outliers / zero keys")
     mean_v = f8.dequant_v(store, 1).mean(axis=0)
     assert np.max(np.abs(out[1].cpu().double().numpy() - mean_v[None, :])) < 1e-5
+
+
+def test_attend_f8_calls_on_one_output_stay_in_stream_order(cuda):
+    # as for kvi8r: chained launches inside a call, but each call's first
+    # launch waits for the previous call on the same output
+    b = _b()
+    q, k, v = synth.make_qkv(2, 2500, seed=42, k_outliers=True, device=cuda)
+    st1 = b.build_store_f8(k, v)
+    st2 = b.build_store_f8(v, k)
+    ref2 = b.attend_f8(q, st2, q_chunk=2500, kv_block=1024)
+    o = torch.empty_like(ref2)
+    for _ in range(3):
+        b.attend_f8(q, st1, q_chunk=256, kv_block=1024, out=o)
+        b.attend_f8(q, st2, q_chunk=600, kv_block=1024, out=o)
+    b.sync_status()
+    assert torch.equal(o, ref2)
