@@ -593,9 +593,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_qk(1, 0);
         mma_commit(smem_u32(&sm.s_full[1]));
         mma_commit(smem_u32(&sm.k_free[0]));
+        // position inside the kv_block: a counter on the exact path (3.5 %
+        // faster there), the division on kvi8r (1.2 % faster there: its issue
+        // warpgroup runs in 72 registers beside the dequantisers)
+        int jb = 0;
         for (int j = 0; j < n_tiles && ok; ++j) {
           const int vs = j % kNV;
-          const bool acc = (j % blk) != 0;
+          const bool acc = kKvi8r ? (j % blk) != 0 : jb != 0;
           const bool more = j + 1 < n_tiles;
           const int ks1 = (j + 1) % kNK;
           ok = mbar_wait(smem_u32(&v_rdy[vs]), (j / kNV) & 1, wctx) &&
@@ -618,6 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(smem_u32(&sm.s_full[1]));
             mma_commit(smem_u32(&sm.k_free[ks1]));
           }
+          if constexpr (!kKvi8r) jb = jb + 1 == blk ? 0 : jb + 1;
         }
         if (ok) mma_commit(smem_u32(&sm.o_full));
       }
