@@ -405,9 +405,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_qk(1, 0);
         mma_commit(smem_u32(&sm.s_full[1]));
         mma_commit(smem_u32(&sm.k_free[0]));
+        int jb = 0;  // j mod kv_block_tiles, kept by a counter (no division in the issue loop)
         for (int j = 0; j < n_tiles && ok; ++j) {
           const int vs = j % kNV;
-          const bool acc = (j % blk) != 0;
+          const bool acc = jb != 0;
           const bool more = j + 1 < n_tiles;
           const int ks1 = (j + 1) % kNK;
           ok = mbar_wait(smem_u32(&sm.v_full[vs]), (j / kNV) & 1, wctx) &&
@@ -430,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(smem_u32(&sm.s_full[1]));
             mma_commit(smem_u32(&sm.k_free[ks1]));
           }
+          jb = jb + 1 == blk ? 0 : jb + 1;
         }
         if (ok) mma_commit(smem_u32(&sm.o_full));
       }
