@@ -16,12 +16,13 @@ from store_h3kv_build_gb300 import binding as b  # noqa: E402  (built by conftes
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(h3kv_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(h3kv_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_every_declared_symbol_is_exported():
     names = declared_functions()
-    assert len(names) >= 7
+    assert len(names) == 18
+    assert {"h3kv_attend_f8", "h3kv_build_store_f8", "h3kv_f8_v_stride", "h3kv_store_f8_bytes"} <= set(names)
     lib = ctypes.CDLL(b.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
