@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the kvi8r and kvf8s stores and attention (test
+"""fp64 CPU oracle for the kvi8r, kvf8s and kvfp4 stores and attention (test
 infrastructure only).
 
 Only the test suite, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
@@ -11,3 +11,4 @@ from .kvi8r import (  # noqa: F401
     attend_exact, attend_blockwise, rel_rms, group_scales, encode_rows_grouped, build_store_grouped,
 )
 from . import kvf8s  # noqa: F401
+from . import kvfp4  # noqa: F401
