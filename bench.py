@@ -64,6 +64,14 @@ def f8_store_bytes(heads, seq):
     return 2 * (2 * rows * HEAD_DIM * 2) + 2 * rows * HEAD_DIM + heads * ((seq + 63) // 64) * 4 + 2 * heads * 512
 
 
+def fp4_store_bytes(heads, seq):
+    """Algorithmic bytes of one kvfp4 store build: read bf16 K and V, write
+    packed e2m1 codes (64 bytes a row) and e4m3 block scales (8 a row) for
+    both: 0.5625 byte per stored element."""
+    rows = heads * seq
+    return 2 * rows * HEAD_DIM * 2 + 2 * rows * (64 + 8)
+
+
 def workload_desc(name, w):
     return {
         "workload": f"{name}: {w['heads']} heads x {w['seq']} tokens x d{HEAD_DIM}, bf16 Q/K/V ~N(0,1)"
@@ -193,6 +201,26 @@ def time_oracle_sample_f8(w, rows=256, seed=0):
     att = attention_flops(1, rows, w["seq"]) / (t2 - t1) / 1e12
     gbs = f8_store_bytes(1, w["seq"]) / (t1 - t0) / 1e9
     desc = (f"kvf8s oracle (NumPy fp64): store of 1 head x {w['seq']} tokens, then {rows} query rows of that "
+            f"head attended over all {w['seq']} keys")
+    return att, gbs, t2 - t0, desc
+
+
+def time_oracle_sample_fp4(w, rows=256, seed=0):
+    """The kvfp4 oracle on a bounded sample: the store of one head (all
+    `seq` tokens) and `rows` query rows of that head attended over it.
+    Returns (attention TFLOP/s, store GB/s, seconds, desc)."""
+    from oracle import kvfp4 as f4
+    q = synth.normal_bf16((1, rows, HEAD_DIM), seed + 100)
+    k = synth.make_k(1, w["seq"], seed + 101, w["k_outliers"])
+    v = synth.normal_bf16((1, w["seq"], HEAD_DIM), seed + 102)
+    t0 = time.perf_counter()
+    st = f4.build_store_kvfp4(k, v)
+    t1 = time.perf_counter()
+    f4.attend_kvfp4(q, st)
+    t2 = time.perf_counter()
+    att = attention_flops(1, rows, w["seq"]) / (t2 - t1) / 1e12
+    gbs = fp4_store_bytes(1, w["seq"]) / (t1 - t0) / 1e9
+    desc = (f"kvfp4 oracle (NumPy fp64): store of 1 head x {w['seq']} tokens, then {rows} query rows of that "
             f"head attended over all {w['seq']} keys")
     return att, gbs, t2 - t0, desc
 
@@ -398,6 +426,23 @@ def run_ours(args, w, name):
     f8_bytes = f8_store_bytes(H, L)
     del fst
 
+    # ---- the kvfp4 store (NVFP4 K/V: e2m1 with one e4m3 scale per 16,
+    # dequantised exactly to fp16 for the tensor cores) on the same inputs
+    pst = b.StoreFp4.empty(H, L, dev)
+    b.build_store_fp4(k, v, out=pst)
+    b.attend_fp4(q, pst, q_chunk=q_chunk, kv_block=kv_block, out=out)
+    ps, pm, pe = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    ps.record(stream)
+    b.build_store_fp4(k, v, out=pst)
+    pm.record(stream)
+    b.attend_fp4(q, pst, q_chunk=q_chunk, kv_block=kv_block, out=out)
+    pe.record(stream)
+    torch.cuda.synchronize(dev)
+    b.sync_status()
+    fp4_build_ms, fp4_attend_ms = ps.elapsed_time(pm), pm.elapsed_time(pe)
+    fp4_bytes = fp4_store_bytes(H, L)
+    del pst
+
     # ---- the same store held in pinned Grace memory and staged into HBM one
     # kv_block at a time (the pages keep kv_block for a host-staged K/V design)
     hst = b.Store.empty(H, L, host=True)
@@ -445,6 +490,14 @@ def run_ours(args, w, name):
                          "attend_frac_of_fp8_peak": flops / (f8_attend_ms / 1e3) / 1e12 / (2 * peak),
                          "fp8_peak_source": f"{peak_src} bf16_tflops_sustained x 2 (nominal fp8/bf16 dense "
                                             "ratio 4.5/2.25 PFLOP/s)"},
+            "fp4_store": {"what": "kvfp4: NVFP4 K/V (e2m1, one e4m3 scale per 16 values; K rotated), each "
+                                  "block dequantised exactly to fp16 for kind::f16 MMAs",
+                          "attend_ms": fp4_attend_ms, "attend_tflops": flops / (fp4_attend_ms / 1e3) / 1e12,
+                          "attend_frac": flops / (fp4_attend_ms / 1e3) / 1e12 / peak,
+                          "build_ms": fp4_build_ms, "build_bytes": fp4_bytes,
+                          "build_gbs": fp4_bytes / (fp4_build_ms / 1e3) / 1e9,
+                          "build_frac_of_hbm": fp4_bytes / (fp4_build_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                          "store_bytes": 2 * H * L * (64 + 8)},
             "host_store": {"where": "kvi8r store built into pinned Grace memory over NVLink-C2C, attended "
                                     "with h3kv_attend_staged (each kv_block copied into HBM, copies timed)",
                            "attend_ms": host_attend_ms, "attend_tflops": flops / (host_attend_ms / 1e3) / 1e12,
@@ -472,6 +525,10 @@ def run_ours(args, w, name):
             line["f8_store"]["cpu_baseline"] = {"value": att8, "unit": UNIT, "cores": blas_threads(),
                                                 "kind": "oracle", "sample": desc8, "store_gbs": gbs8,
                                                 "seconds": s8}
+            att4, gbs4, s4, desc4 = time_oracle_sample_fp4(w)
+            line["fp4_store"]["cpu_baseline"] = {"value": att4, "unit": UNIT, "cores": blas_threads(),
+                                                 "kind": "oracle", "sample": desc4, "store_gbs": gbs4,
+                                                 "seconds": s4}
         print(json.dumps(line), flush=True)
     if dist:
         import torch.distributed as tdist

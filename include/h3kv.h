@@ -1,8 +1,9 @@
 /*
  * h3kv.h -- C ABI of libh3kv: the kvi8r rotated-int8 whole-sequence K/V store
  * and query-chunked attention over it, on one NVIDIA GB300 (sm_103a); the
- * exact bf16 comparison path; and the kvf8s store (fp8 e4m3 in the kvi8s
- * layout) attended on the fp8 tensor path.
+ * exact bf16 comparison path; the kvf8s store (fp8 e4m3 in the kvi8s
+ * layout) attended on the fp8 tensor path; and the kvfp4 store (NVFP4 K/V)
+ * dequantised exactly to fp16 for the tensor cores.
  *
  * Source of the method: "H3 Streamed Blocks (exact low-VRAM, alpha)", Inputs
  * table (kv_store, q_chunk, kv_block rows), and "Low VRAM, low RAM: the
@@ -38,7 +39,7 @@
 extern "C" {
 #endif
 
-#define H3KV_ABI_VERSION 3u
+#define H3KV_ABI_VERSION 4u
 #define H3KV_HEAD_DIM 128
 /* kv_block = 0 on the kvi8r path means this many tokens (the kv_block
  * default of the kv_store row). */
@@ -254,6 +255,51 @@ h3kv_status h3kv_build_store_f8(const uint16_t *K, const uint16_t *V, int32_t he
  *   bit-identical for every q_chunk.  store->heads <= 65535. */
 h3kv_status h3kv_attend_f8(const uint16_t *Q, int64_t q_seq, const h3kv_store_f8 *store, int32_t q_chunk,
                            int32_t kv_block, float softmax_scale, float *O, void *stream);
+
+/* ------------------------------------------------------------------ kvfp4
+ * The kvfp4 store: kvfp4s of the kv_store row of the H3 Streamed Blocks
+ * Inputs table -- K/V kept as NVFP4 (e2m1 values with one e4m3 scale per 16
+ * elements, 0.5625 byte per element), Q and K Hadamard-rotated, no K
+ * smoothing and no query centring.  e2m1 has 1 sign, 2 exponent (bias 1) and
+ * 1 mantissa bit: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.  e4m3 as for kvf8s.
+ * For each (head, token) row x -- of K rotated (x = k H, the kvi8r basis) or
+ * of V (not rotated) -- and each block B of 16 consecutive values:
+ *   s_B = e4m3_rne(max_{j in B} |x_j| / 6)        (saturating at 448),
+ *   c_j = e2m1_rne(x_j / s_B), sign of x_j        (saturating at +-6),
+ *   every c_j = 0 where s_B == 0.
+ * Codes are packed two per byte, element 2i in the low nibble of byte i.
+ * Dequantisation c_j s_B is exact in fp16.  Every buffer is caller-owned
+ * device memory, 16-byte aligned. */
+typedef struct {
+  uint8_t *k_codes;  /* e2m1 pairs [heads, seq, 64] */
+  uint8_t *v_codes;  /* e2m1 pairs [heads, seq, 64] */
+  uint8_t *k_scales; /* e4m3 [heads, seq, 8] */
+  uint8_t *v_scales; /* e4m3 [heads, seq, 8] */
+  int32_t heads;
+  int64_t seq;
+  int32_t head_dim;  /* must be 128 */
+} h3kv_store_fp4;
+
+/* Bytes of a kvfp4 store's four buffers together, 2 heads seq (64 + 8) (0
+ * for invalid arguments). */
+size_t h3kv_store_fp4_bytes(int32_t heads, int64_t seq, int32_t head_dim);
+
+/* Build the kvfp4 store of bf16 K and V [heads, seq, 128] into `out`, whose
+ * heads/seq/head_dim must match.  One stream-ordered pass; rows are
+ * independent, so the store is the same on every run. */
+h3kv_status h3kv_build_store_fp4(const uint16_t *K, const uint16_t *V, int32_t heads, int64_t seq,
+                                 int32_t head_dim, const h3kv_store_fp4 *out, void *stream);
+
+/* kvfp4 attention: q' = fp16(Q H); each K/V block of the store dequantised
+ * to fp16 (exactly); S = q' K^T softmax_scale with fp32 accumulation;
+ * P = softmax(S) over all store->seq keys (non-causal), in kv_block-token
+ * blocks combined by their log-sum-exp, entering P.V as fp16; O = P V in
+ * fp32.  V is not rotated, so O needs no un-rotation.
+ *   Q: bf16 [store->heads, q_seq, 128].  O: fp32 [store->heads, q_seq, 128].
+ *   q_chunk, kv_block and softmax_scale as for h3kv_attend; the output is
+ *   bit-identical for every q_chunk. */
+h3kv_status h3kv_attend_fp4(const uint16_t *Q, int64_t q_seq, const h3kv_store_fp4 *store, int32_t q_chunk,
+                            int32_t kv_block, float softmax_scale, float *O, void *stream);
 
 /* Synchronise `stream`, then return and clear the device error word that the
  * kernels set when a bounded wait runs out (H3KV_ERR_DEVICE_TIMEOUT), or

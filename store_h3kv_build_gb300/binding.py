@@ -55,6 +55,18 @@ class h3kv_store_f8(ctypes.Structure):  # noqa: N801 - mirrors the C struct name
     ]
 
 
+class h3kv_store_fp4(ctypes.Structure):  # noqa: N801 - mirrors the C struct name
+    _fields_ = [
+        ("k_codes", ctypes.c_void_p),
+        ("v_codes", ctypes.c_void_p),
+        ("k_scales", ctypes.c_void_p),
+        ("v_scales", ctypes.c_void_p),
+        ("heads", ctypes.c_int32),
+        ("seq", ctypes.c_int64),
+        ("head_dim", ctypes.c_int32),
+    ]
+
+
 _vp, _i32, _i64, _f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
 _SIGS = {
     "h3kv_abi_version": (ctypes.c_uint32, []),
@@ -75,6 +87,9 @@ _SIGS = {
     "h3kv_store_f8_bytes": (ctypes.c_size_t, [_i32, _i64, _i32]),
     "h3kv_build_store_f8": (ctypes.c_int, [_vp, _vp, _i32, _i64, _i32, ctypes.POINTER(h3kv_store_f8), _vp]),
     "h3kv_attend_f8": (ctypes.c_int, [_vp, _i64, ctypes.POINTER(h3kv_store_f8), _i32, _i32, _f32, _vp, _vp]),
+    "h3kv_store_fp4_bytes": (ctypes.c_size_t, [_i32, _i64, _i32]),
+    "h3kv_build_store_fp4": (ctypes.c_int, [_vp, _vp, _i32, _i64, _i32, ctypes.POINTER(h3kv_store_fp4), _vp]),
+    "h3kv_attend_fp4": (ctypes.c_int, [_vp, _i64, ctypes.POINTER(h3kv_store_fp4), _i32, _i32, _f32, _vp, _vp]),
     "h3kv_set_wait_timeout_ns": (ctypes.c_int, [ctypes.c_uint64]),
     "h3kv_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _vp]),
     "h3kv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -278,6 +293,51 @@ def attend_f8(Q: torch.Tensor, store: StoreF8, q_chunk: int = 16384, kv_block: i
     st = store.c_struct()
     check(h3kv_attend_f8(_ptr(Q), q_seq, ctypes.byref(st), int(q_chunk), int(kv_block), float(softmax_scale),
                          _ptr(out), _stream(stream)), "h3kv_attend_f8")
+    return out
+
+
+class StoreFp4:
+    """A kvfp4 store held in torch tensors: packed e2m1 codes [heads, seq, 64]
+    (uint8, element 2i in the low nibble of byte i) and e4m3 block scales
+    [heads, seq, 8] (uint8) for K and for V."""
+
+    def __init__(self, k_codes, v_codes, k_scales, v_scales):
+        self.k_codes, self.v_codes = k_codes, v_codes
+        self.k_scales, self.v_scales = k_scales, v_scales
+        self.heads, self.seq = int(k_codes.shape[0]), int(k_codes.shape[1])
+
+    @classmethod
+    def empty(cls, heads: int, seq: int, device="cuda") -> "StoreFp4":
+        kc = torch.empty((heads, seq, HEAD_DIM // 2), dtype=torch.uint8, device=device)
+        ks = torch.empty((heads, seq, HEAD_DIM // 16), dtype=torch.uint8, device=device)
+        return cls(kc, torch.empty_like(kc), ks, torch.empty_like(ks))
+
+    def c_struct(self) -> h3kv_store_fp4:
+        return h3kv_store_fp4(_ptr(self.k_codes), _ptr(self.v_codes), _ptr(self.k_scales), _ptr(self.v_scales),
+                              self.heads, self.seq, HEAD_DIM)
+
+    def nbytes(self) -> int:
+        return int(h3kv_store_fp4_bytes(self.heads, self.seq, HEAD_DIM))
+
+
+def build_store_fp4(K: torch.Tensor, V: torch.Tensor, out: StoreFp4 | None = None, stream=None) -> StoreFp4:
+    """h3kv_build_store_fp4 on bf16 K, V [heads, seq, 128] (CUDA, contiguous)."""
+    heads, seq = int(K.shape[0]), int(K.shape[1])
+    out = StoreFp4.empty(heads, seq, K.device) if out is None else out
+    st = out.c_struct()
+    check(h3kv_build_store_fp4(_ptr(K), _ptr(V), heads, seq, int(K.shape[2]), ctypes.byref(st), _stream(stream)),
+          "h3kv_build_store_fp4")
+    return out
+
+
+def attend_fp4(Q: torch.Tensor, store: StoreFp4, q_chunk: int = 16384, kv_block: int = 0,
+               softmax_scale: float = 0.0, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """h3kv_attend_fp4: kvfp4 attention of bf16 Q [heads, q_seq, 128] -> fp32."""
+    q_seq = int(Q.shape[1])
+    out = torch.empty(Q.shape, dtype=torch.float32, device=Q.device) if out is None else out
+    st = store.c_struct()
+    check(h3kv_attend_fp4(_ptr(Q), q_seq, ctypes.byref(st), int(q_chunk), int(kv_block), float(softmax_scale),
+                          _ptr(out), _stream(stream)), "h3kv_attend_fp4")
     return out
 
 

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libh3kv.so")
 SOURCES = ["abi.cu", "store_build.cu", "attend_kvi8r.cu", "attend_exact.cu", "attend_static_scratch.cu",
-           "store_f8.cu", "attend_f8.cu"]
+           "store_f8.cu", "attend_f8.cu", "store_fp4.cu", "attend_fp4.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "-Xptxas", "-v", "-I", os.path.join(os.path.dirname(HERE), "include")]

@@ -123,6 +123,18 @@ bool encode_3d_u8(CUtensorMap *m, const void *base, uint64_t inner, uint64_t mid
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over kvfp4 codes [rows, 64 bytes]: box 64 x 128 rows with the
+// 64-byte swizzle (the store build's staging layout).
+bool encode_codes_fp4(CUtensorMap *m, const void *base, uint64_t rows) {
+  const cuuint64_t dims[2] = {64, rows};
+  const cuuint64_t strides[1] = {64};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // TMA coordinates are signed 32-bit; keep every row index below 2^31.
 constexpr int64_t kMaxRows = (1ll << 31) - 256;
 
@@ -541,6 +553,81 @@ h3kv_status h3kv_attend_f8(const uint16_t *Q, int64_t q_seq, const h3kv_store_f8
     a.q_begin = c0;
     a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
     if (h3kv::launch_attend_f8(tk, tv, a, c0 > 0, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return H3KV_ERR_CUDA;
+  }
+  return H3KV_OK;
+}
+
+size_t h3kv_store_fp4_bytes(int32_t heads, int64_t seq, int32_t head_dim) {
+  if (heads < 0 || seq < 0 || head_dim != H3KV_HEAD_DIM) return 0;
+  return 2 * static_cast<size_t>(heads) * static_cast<size_t>(seq) * (64 + 8);
+}
+
+h3kv_status h3kv_build_store_fp4(const uint16_t *K, const uint16_t *V, int32_t heads, int64_t seq,
+                                 int32_t head_dim, const h3kv_store_fp4 *out, void *stream) {
+  if (heads < 0 || seq < 0 || !out) return H3KV_ERR_INVALID_ARG;
+  if (head_dim != H3KV_HEAD_DIM || out->head_dim != H3KV_HEAD_DIM) return H3KV_ERR_UNSUPPORTED;
+  if (out->heads != heads || out->seq != seq) return H3KV_ERR_INVALID_ARG;
+  const int64_t rows = static_cast<int64_t>(heads) * seq;
+  if (rows == 0) return H3KV_OK;
+  if (rows > kMaxRows) return H3KV_ERR_INVALID_ARG;
+  if (!K || !V || !out->k_codes || !out->v_codes || !out->k_scales || !out->v_scales) return H3KV_ERR_INVALID_ARG;
+  if (!aligned16(K) || !aligned16(V) || !aligned16(out->k_codes) || !aligned16(out->v_codes) ||
+      !aligned16(out->k_scales) || !aligned16(out->v_scales))
+    return H3KV_ERR_INVALID_ARG;
+  DeviceInfo *d = nullptr;
+  h3kv_status st = device_info(&d);
+  if (st != H3KV_OK) return st;
+  CUtensorMap k_in, v_in, k_out, v_out;
+  if (!encode_2d(&k_in, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, rows, 2, 64) ||
+      !encode_2d(&v_in, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, 2, 64) ||
+      !encode_codes_fp4(&k_out, out->k_codes, rows) || !encode_codes_fp4(&v_out, out->v_codes, rows))
+    return H3KV_ERR_CUDA;
+  const cudaError_t e = h3kv::launch_store_build_fp4(k_in, v_in, k_out, v_out, out->k_scales, out->v_scales, rows,
+                                                     d->num_sms, d->err, g_timeout_ns.load(),
+                                                     static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? H3KV_OK : H3KV_ERR_CUDA;
+}
+
+h3kv_status h3kv_attend_fp4(const uint16_t *Q, int64_t q_seq, const h3kv_store_fp4 *store, int32_t q_chunk,
+                            int32_t kv_block, float softmax_scale, float *O, void *stream) {
+  if (!store || q_seq < 0 || store->heads < 0 || store->seq < 0) return H3KV_ERR_INVALID_ARG;
+  if (store->head_dim != H3KV_HEAD_DIM) return H3KV_ERR_UNSUPPORTED;
+  h3kv_status st = check_chunks(q_chunk, kv_block);
+  if (st != H3KV_OK) return st;
+  if (store->heads == 0 || q_seq == 0) return H3KV_OK;
+  if (store->seq == 0) return H3KV_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(store->heads) * q_seq > kMaxRows || static_cast<int64_t>(store->heads) * store->seq > kMaxRows)
+    return H3KV_ERR_INVALID_ARG;
+  if (!Q || !O || !store->k_codes || !store->v_codes || !store->k_scales || !store->v_scales)
+    return H3KV_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(O) || !aligned16(store->k_codes) || !aligned16(store->v_codes) ||
+      !aligned16(store->k_scales) || !aligned16(store->v_scales))
+    return H3KV_ERR_INVALID_ARG;
+  DeviceInfo *d = nullptr;
+  st = device_info(&d);
+  if (st != H3KV_OK) return st;
+  const int32_t kvb = kv_block == 0 ? H3KV_DEFAULT_KV_BLOCK : kv_block;
+  h3kv::AttnArgs a{};
+  a.q = Q;
+  a.k_codes = reinterpret_cast<const int8_t *>(store->k_codes);
+  a.v_codes = reinterpret_cast<const int8_t *>(store->v_codes);
+  a.k_fp4_scales = store->k_scales;
+  a.v_fp4_scales = store->v_scales;
+  a.o = O;
+  a.q_seq = q_seq;
+  a.kv_seq = store->seq;
+  a.kv_stride = store->seq;
+  a.scale_groups = 1;
+  a.heads = store->heads;
+  a.kv_block_tiles = kvb / H3KV_KV_TILE;
+  a.scale_log2 = scale_log2_of(softmax_scale);
+  a.err = d->err;
+  a.timeout_ns = g_timeout_ns.load();
+  for (int64_t c0 = 0; c0 < q_seq; c0 += q_chunk) {
+    a.q_begin = c0;
+    a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
+    if (h3kv::launch_attend_fp4(a, c0 > 0, static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return H3KV_ERR_CUDA;
   }
   return H3KV_OK;

@@ -9,7 +9,11 @@
 // scale, scores and P.V run in fp16 with fp32 accumulation, blocks of
 // kv_block keys are combined by their log-sum-exp, and the output is
 // un-rotated once (O = O' H^T).  The exact store runs the same pipeline on
-// bf16 K/V without rotation or dequantisation.
+// bf16 K/V without rotation or dequantisation.  The kvfp4 store (kvfp4s in
+// the same kv_store row: NVFP4 K/V, e2m1 values with one e4m3 scale per 16,
+// Q and K rotated) runs the kvi8r pipeline with each block dequantised as
+// e2m1 -> fp16 times its e4m3 scale -- exact in fp16 -- and no un-rotation,
+// V not being rotated.
 //
 // One CTA owns 256 query rows of one head (two 128-row tiles, so that the
 // softmax of one tile overlaps the tensor-core work of the other) and walks
@@ -19,7 +23,8 @@
 // Warp roles (512 threads):
 //   warps 0-3   softmax / correction / epilogue of query tile 0 (thread = row)
 //   warps 4-7   the same for query tile 1
-//   warps 8-11  kvi8r: in-place int8 -> fp16 dequantisation of K and V tiles
+//   warps 8-11  kvi8r / kvfp4: in-place int8 (e2m1) -> fp16 dequantisation
+//               of K and V tiles
 //   warp 12     producer: TMA / bulk copies of Q (exact) and K/V tiles
 //   warp 13     TMEM allocation and tcgen05.mma issue (one thread)
 //   warps 14-15 idle
@@ -146,6 +151,67 @@ __device__ __forceinline__ void dequant_tile(uint8_t *tile, const uint16_t (&sc)
   }
 }
 
+// kvfp4: one 16-value block (8 code bytes, element 2i in the low nibble of
+// byte i) -> 16 fp16 values code * scale.  Both conversions are exact, and so
+// is the product: a 2-bit times a 4-bit significand, at most 2688 in size.
+__device__ __forceinline__ void dequant16_fp4(const uint2 raw, uint32_t s2, uint32_t (&out)[8]) {
+  uint32_t a[4], b[4];
+  e2m1x8_to_f16x2(raw.x, a);
+  e2m1x8_to_f16x2(raw.y, b);
+  const __half2 s = *reinterpret_cast<const __half2 *>(&s2);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const __half2 ha = __hmul2(*reinterpret_cast<const __half2 *>(&a[k]), s);
+    const __half2 hb = __hmul2(*reinterpret_cast<const __half2 *>(&b[k]), s);
+    out[k] = *reinterpret_cast<const uint32_t *>(&ha);
+    out[4 + k] = *reinterpret_cast<const uint32_t *>(&hb);
+  }
+}
+
+// kvfp4: e4m3 scales of the blocks this lane dequantises (the lane's
+// granule index is its block within the row), byte `it` of the pair of
+// words for iteration `it`; rows past `valid` get 0.
+__device__ __forceinline__ void dequant_scales_fp4(const uint8_t *scales, int valid, int dw, int lane,
+                                                   uint32_t (&sc)[2]) {
+  const int g = static_cast<int>(dq_granule(lane));
+  sc[0] = sc[1] = 0u;
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int r = static_cast<int>(dq_row(dw, it, lane));
+    const uint32_t b = r < valid ? scales[r * 8 + g] : 0u;
+    sc[it >> 2] |= b << ((it & 3) * 8);
+  }
+}
+
+// kvfp4 dequantisation of one K or V tile by the 128 dequant threads.  The
+// packed codes sit linearly (64 bytes per row) at the start of the buffer,
+// under fp16 output rows of other warps, so every thread first loads its
+// codes, the four warps meet at named barrier 1 (which also ANDs the load
+// waits' outcomes: every warp reaches it whether or not its wait succeeded),
+// and only then does any thread write.  Returns false, having written
+// nothing, when some warp's wait ran out.  Output layout as dequant_tile.
+__device__ __forceinline__ bool dequant_tile_fp4(uint8_t *tile, bool loaded, const uint32_t (&sc)[2], int dw,
+                                                 int lane) {
+  const uint32_t g = dq_granule(lane);
+  uint2 raw[8];
+#pragma unroll
+  for (int it = 0; it < 8; ++it)
+    raw[it] = loaded ? *reinterpret_cast<const uint2 *>(tile + dq_row(dw, it, lane) * 64 + g * 8) : make_uint2(0u, 0u);
+  if (!named_bar_and(1, 128, loaded)) return false;
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const uint32_t r = dq_row(dw, it, lane);
+    uint32_t o[8];
+    // the iteration's scale byte twice: the fp16 pair (s, s)
+    dequant16_fp4(raw[it], e4m3x2_to_f16x2(__byte_perm(sc[it >> 2], 0u, (it & 3) * 0x11u)), o);
+    uint8_t *half_base = tile + (g >> 2) * kChunkBytes;
+    const uint32_t G0 = (g & 3) * 2;
+    *reinterpret_cast<uint4 *>(half_base + sw128_off(r, G0)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4 *>(half_base + sw128_off(r, G0 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+  return true;
+}
+
 // Log-sum-exp merge of a finished block (m_b, l_b) into the running (M, Lam)
 // (max in raw score units, c2 = softmax scale * log2 e): returns the weights
 // of the running and the block output and updates (M, Lam).  Written with
@@ -166,7 +232,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   else return pack_bf16x2(lo, hi);
 }
 
-template <bool kKvi8r, int kGroups>
+template <bool kKvi8r, int kGroups, bool kFp4 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
@@ -460,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ti = wq * 32 + rr;
         const float4 v = *reinterpret_cast<const float4 *>(stage + ti * 512 + ((lane ^ (ti & 31)) << 4));
         float x[4] = {v.x, v.y, v.z, v.w};
-        if constexpr (kKvi8r) {
+        if constexpr (kKvi8r && !kFp4) {
           fwht128_warp(x, lane);
 #pragma unroll
           for (int t = 0; t < 4; ++t) x[t] *= kInvSqrt128;
@@ -475,7 +541,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 12) {
     // ======================================================= dequantisers
     reg_dealloc<kKvi8r ? kRegDequantKvi8r : kRegDequantExact>();
-    if constexpr (kKvi8r) {
+    if constexpr (kFp4) {
+      const int dw = warp - 8;
+      const uint8_t *ksc = a.k_fp4_scales + static_cast<int64_t>(h) * a.kv_stride * 8;
+      const uint8_t *vsc = a.v_fp4_scales + static_cast<int64_t>(h) * a.kv_stride * 8;
+      uint32_t sck[2], scv[2];
+      for (int j = 0; j < n_tiles; ++j) {
+        const int64_t tok0 = static_cast<int64_t>(j) * kBN;
+        const int valid = static_cast<int>(a.kv_seq - tok0 < kBN ? a.kv_seq - tok0 : kBN);
+        const int ks = j % kNK, vs = j % kNV;
+        dequant_scales_fp4(ksc + tok0 * 8, valid, dw, lane, sck);
+        dequant_scales_fp4(vsc + tok0 * 8, valid, dw, lane, scv);
+        if (!dequant_tile_fp4(sm.k[ks], warp_wait(smem_u32(&sm.k_load[ks]), (j / kNK) & 1, wctx), sck, dw, lane))
+          break;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.k_ready[ks]));
+        if (!dequant_tile_fp4(sm.v[vs], warp_wait(smem_u32(&sm.v_load[vs]), (j / kNV) & 1, wctx), scv, dw, lane))
+          break;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.v_ready[vs]));
+      }
+    } else if constexpr (kKvi8r) {
       const int dw = warp - 8;
       const uint16_t *ksc = a.k_scales + static_cast<int64_t>(h) * a.kv_stride * kGroups;
       const uint16_t *vsc = a.v_scales + static_cast<int64_t>(h) * a.kv_stride * kGroups;
@@ -522,7 +610,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(smem_u32(&sm.k_free[ks]), ((j / kNK) & 1) ^ 1, wctx)) break;
         {
           const uint32_t bar = smem_u32(&sm.k_load[ks]);
-          if constexpr (kKvi8r) {
+          if constexpr (kFp4) {
+            const uint32_t bytes = static_cast<uint32_t>((a.kv_seq - tok0 < kBN ? a.kv_seq - tok0 : kBN) * 64);
+            mbar_arrive_expect_tx(bar, bytes);
+            bulk_g2s(smem_u32(sm.k[ks]), a.k_codes + (static_cast<int64_t>(h) * a.kv_stride + tok0) * 64, bytes, bar);
+          } else if constexpr (kKvi8r) {
             const uint32_t bytes = static_cast<uint32_t>((a.kv_seq - tok0 < kBN ? a.kv_seq - tok0 : kBN) * 128);
             mbar_arrive_expect_tx(bar, bytes);
             bulk_g2s(smem_u32(sm.k[ks] + kChunkBytes), a.k_codes + (static_cast<int64_t>(h) * a.kv_stride + tok0) * 128,
@@ -537,7 +629,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(smem_u32(&sm.v_free[vs]), ((j / kNV) & 1) ^ 1, wctx)) break;
         {
           const uint32_t bar = smem_u32(&sm.v_load[vs]);
-          if constexpr (kKvi8r) {
+          if constexpr (kFp4) {
+            const uint32_t bytes = static_cast<uint32_t>((a.kv_seq - tok0 < kBN ? a.kv_seq - tok0 : kBN) * 64);
+            mbar_arrive_expect_tx(bar, bytes);
+            bulk_g2s(smem_u32(sm.v[vs]), a.v_codes + (static_cast<int64_t>(h) * a.kv_stride + tok0) * 64, bytes, bar);
+          } else if constexpr (kKvi8r) {
             const uint32_t bytes = static_cast<uint32_t>((a.kv_seq - tok0 < kBN ? a.kv_seq - tok0 : kBN) * 128);
             mbar_arrive_expect_tx(bar, bytes);
             bulk_g2s(smem_u32(sm.v[vs] + kChunkBytes), a.v_codes + (static_cast<int64_t>(h) * a.kv_stride + tok0) * 128,

@@ -22,10 +22,12 @@ cudaError_t launch_store_build(const CUtensorMap &k_in, const CUtensorMap &v_in,
 
 struct AttnArgs {
   const uint16_t *q;        // bf16 [heads, q_seq, 128]
-  const int8_t *k_codes;    // kvi8r store (unused by the exact path)
-  const int8_t *v_codes;
+  const int8_t *k_codes;    // kvi8r store (unused by the exact path); kvfp4:
+  const int8_t *v_codes;    //   packed e2m1 pairs, 64 bytes per row
   const uint16_t *k_scales;
   const uint16_t *v_scales;
+  const uint8_t *k_fp4_scales;  // kvfp4: e4m3, 8 per row (one per 16 values)
+  const uint8_t *v_fp4_scales;
   float *o;                 // fp32 [heads, q_seq, 128]
   int64_t q_seq;
   int64_t kv_seq;           // keys attended by this launch
@@ -57,6 +59,18 @@ constexpr int kAttnRowsPerCta = 256;  // two 128-row query tiles per CTA
 // for a launch that touches nothing the previous kernel writes (the next
 // query chunk of the same call); the kernels keep completion in stream order.
 cudaError_t launch_attend_kvi8r(const AttnArgs &args, bool overlap_previous, cudaStream_t stream);
+
+// kvfp4 store build: K rotated, V not; per 16-value block an e4m3 scale and
+// e2m1 codes.  Tensor maps: bf16 [rows, 128] inputs (box 64 x 128, 128B
+// swizzle) and u8 [rows, 64] code outputs (box 64 x 128, 64B swizzle).
+cudaError_t launch_store_build_fp4(const CUtensorMap &k_in, const CUtensorMap &v_in, const CUtensorMap &k_out,
+                                   const CUtensorMap &v_out, uint8_t *k_scales, uint8_t *v_scales, int64_t rows,
+                                   int num_sms, uint32_t *err, uint64_t timeout_ns, cudaStream_t stream);
+
+// kvfp4 attention over [q_begin, q_end): the kvi8r kernel with the store's
+// K/V blocks dequantised from e2m1 x e4m3 (exact in fp16) and no output
+// un-rotation (V is not rotated).
+cudaError_t launch_attend_fp4(const AttnArgs &args, bool overlap_previous, cudaStream_t stream);
 
 // kvf8s store build: statistics pass (K mean, V channel absmax) then the
 // encode pass.  V codes are written channel-major with row stride v_stride

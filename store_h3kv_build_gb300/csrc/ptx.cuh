@@ -408,6 +408,50 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
+// fp32 -> one e4m3 byte (round to nearest even, saturating at +-448).
+__device__ __forceinline__ uint32_t f32_to_e4m3(float x) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.f), "f"(x));
+  return r & 0xFFu;
+}
+
+// Two e4m3 bytes (the low 16 bits of `two`) -> an fp16 pair, the low byte
+// in the low half; exact (every e4m3 value is an fp16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<uint16_t>(two)));
+  return r;
+}
+
+// One e4m3 byte -> the fp16 pair (v, v).
+__device__ __forceinline__ uint32_t e4m3_to_f16x2_dup(uint32_t byte) { return e4m3x2_to_f16x2(byte * 0x101u); }
+
+// Four fp32 values -> four e2m1 nibbles (round to nearest even, saturating
+// at +-6), value a in the lowest nibble.
+__device__ __forceinline__ uint32_t pack_e2m1x4(float a, float b, float c, float d) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 lo, hi;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 hi, %4, %3;\n\t"
+      "mov.b16 %0, {lo, hi};\n\t}"
+      : "=h"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
+  return r;
+}
+
+// Eight e2m1 nibbles (element 0 in the lowest) -> four fp16 pairs, element
+// 2i in the low half of word i; exact.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&o)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
+}
+
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

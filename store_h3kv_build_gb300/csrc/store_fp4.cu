@@ -1,0 +1,229 @@
+// store_fp4.cu -- the kvfp4 store build (kv_store row of the H3 Streamed
+// Blocks Inputs table, kvfp4s: K/V as NVFP4 -- e2m1 values with one e4m3
+// scale per 16 elements -- with Q and K Hadamard-rotated): every (token,
+// head) row of K is rotated by the fixed orthonormal 128-wide Hadamard basis,
+// V is not; each 16-value block of a row gets s = e4m3(max|x| / 6) and the
+// codes e2m1(x / s), all zero where s == 0.
+//
+// GB300 design: the HBM-bound stream of the kvi8r build.  A persistent grid
+// walks 128-row tiles (K tiles, then V tiles); one producer warp streams bf16
+// tiles into a 2-stage ring with TMA (128-byte swizzle), four compute warps
+// own one row per thread and write codes into a 64-byte-swizzled tile (16-byte
+// stores conflict free) that one thread stores with a TMA tensor store, and
+// the scales with one bulk copy.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace h3kv {
+namespace {
+
+constexpr int kRows = 128;                  // rows per tile = compute threads
+constexpr int kStages = 2;                  // input ring depth (2 CTAs per SM)
+constexpr int kInTileBytes = kRows * 256;   // bf16 [128 x 128]
+constexpr int kOutCodeBytes = kRows * 64;   // e2m1 pairs [128 x 64 bytes]
+constexpr int kOutScaleBytes = kRows * 8;   // e4m3 [128 x 8]
+constexpr int kThreads = kRows + 32;        // 4 compute warps + 1 producer warp
+
+struct Fp4BuildSmem {
+  uint8_t in[kStages][kInTileBytes];
+  uint8_t out_codes[2][kOutCodeBytes];
+  uint8_t out_scales[2][kOutScaleBytes];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  int abort;
+};
+
+constexpr size_t kFp4BuildSmemBytes = sizeof(Fp4BuildSmem) + 1024;
+
+// Byte offset of 16-byte chunk c (0..3) of row r in a 64-byte-wide tile
+// stored with the 64-byte swizzle (chunk c sits at c ^ ((r / 2) mod 4)).
+__device__ __forceinline__ uint32_t sw64_off(uint32_t r, uint32_t c) { return r * 64u + ((c ^ ((r >> 1) & 3u)) << 4); }
+
+// x / d given r = 1/d rounded to fp32: q0 = x r corrected once by its exact
+// residual (Markstein's division step: e = q0 d - x by one fma, then
+// q0 - e r).  A quotient that is exactly representable -- the only kind that
+// can sit on a rounding midpoint of e2m1 or e4m3 here -- comes out exact, so
+// the nearest-even decision that follows is the one for x / d itself; a zero
+// keeps its sign.
+__device__ __forceinline__ float div_step(float x, float d, float r) {
+  const float q0 = x * r;
+  const float e = fmaf(q0, d, -x);
+  return fmaf(e, -r, q0);
+}
+
+// Codes of one 16-value block x[0..15] with scale s > 0 (r = 1/s rounded to
+// fp32): e2m1 of x / s.  Returns the 16 nibbles in two words, element 0
+// lowest.
+__device__ __forceinline__ uint2 encode_block(const float *x, float s, float r) {
+  float q[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) q[i] = div_step(x[i], s, r);
+  uint2 w;
+  w.x = pack_e2m1x4(q[0], q[1], q[2], q[3]) | (pack_e2m1x4(q[4], q[5], q[6], q[7]) << 16);
+  w.y = pack_e2m1x4(q[8], q[9], q[10], q[11]) | (pack_e2m1x4(q[12], q[13], q[14], q[15]) << 16);
+  return w;
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    store_fp4_kernel(const __grid_constant__ CUtensorMap tm_k_in, const __grid_constant__ CUtensorMap tm_v_in,
+                     const __grid_constant__ CUtensorMap tm_k_out, const __grid_constant__ CUtensorMap tm_v_out,
+                     uint8_t *__restrict__ k_scales, uint8_t *__restrict__ v_scales, int64_t rows,
+                     int64_t tiles_per_tensor, uint32_t *err, uint64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  Fp4BuildSmem &sm =
+      *reinterpret_cast<Fp4BuildSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int64_t total_tiles = 2 * tiles_per_tensor;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&sm.full[s]), 1);
+      mbar_init(smem_u32(&sm.empty[s]), kRows);
+    }
+    sm.abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  WaitCtx wctx{err, &sm.abort, timeout_ns};
+
+  if (warp == 4) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_k_in);
+      prefetch_tmap(&tm_v_in);
+      int it = 0;
+      int issued = 0;
+      for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1;
+        if (!mbar_wait(smem_u32(&sm.empty[s]), ph ^ 1, wctx)) break;
+        const bool is_v = t >= tiles_per_tensor;
+        const int32_t row0 = static_cast<int32_t>((is_v ? t - tiles_per_tensor : t) * kRows);
+        const CUtensorMap *map = is_v ? &tm_v_in : &tm_k_in;
+        const uint32_t bar = smem_u32(&sm.full[s]);
+        mbar_arrive_expect_tx(bar, kInTileBytes);
+        tma_load_2d(smem_u32(&sm.in[s][0]), map, 0, row0, bar);
+        tma_load_2d(smem_u32(&sm.in[s][kInTileBytes / 2]), map, 64, row0, bar);
+        ++issued;
+      }
+      if (sm.abort) {
+        for (int k = (issued > kStages ? issued - kStages : 0); k < issued; ++k)
+          mbar_wait_drain(smem_u32(&sm.full[k % kStages]), (k / kStages) & 1, kDrainNs);
+      }
+    }
+  } else {
+    // ----------------------------------------------------------- compute
+    const uint32_t r = static_cast<uint32_t>(tid);  // row within tile
+    int it = 0;
+    for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+      const int s = it % kStages;
+      const uint32_t ph = (it / kStages) & 1;
+      const int b = it & 1;
+      // output tile b must no longer be read by the stores of tile it-2
+      if (tid == 0) bulk_wait_read<1>();
+      const bool ok = mbar_wait(smem_u32(&sm.full[s]), ph, wctx);
+      if (!named_bar_and(1, kRows, ok)) break;
+
+      float x[128];
+      const uint8_t *tile = sm.in[s];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(tile + c * (kInTileBytes / 2) + sw128_off(r, g));
+          const int e = c * 64 + g * 8;
+          x[e + 0] = bf16lo_to_f32(v.x);
+          x[e + 1] = bf16hi_to_f32(v.x);
+          x[e + 2] = bf16lo_to_f32(v.y);
+          x[e + 3] = bf16hi_to_f32(v.y);
+          x[e + 4] = bf16lo_to_f32(v.z);
+          x[e + 5] = bf16hi_to_f32(v.z);
+          x[e + 6] = bf16lo_to_f32(v.w);
+          x[e + 7] = bf16hi_to_f32(v.w);
+        }
+      }
+      mbar_arrive(smem_u32(&sm.empty[s]));
+
+      const bool is_v = t >= tiles_per_tensor;
+      if (!is_v) {
+        // k' = k H: the unnormalised transform, then 2^-3.5
+        fwht128_packed(x);
+        const float2 inv = make_float2(kInvSqrt128, kInvSqrt128);
+#pragma unroll
+        for (int e = 0; e < 128; e += 2) {
+          const float2 p = __fmul2_rn(make_float2(x[e], x[e + 1]), inv);
+          x[e] = p.x;
+          x[e + 1] = p.y;
+        }
+      }
+
+      uint8_t *oc = sm.out_codes[b];
+      uint32_t sw[2] = {0u, 0u};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        // blocks 2c and 2c + 1 fill 16-byte chunk c of the row's 64 code bytes
+        uint2 w[2];
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          const int blk = 2 * c + hb;
+          const float *xb = x + blk * 16;
+          float am[2] = {0.f, 0.f};
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            am[0] = fmax3(am[0], fabsf(xb[i]), fabsf(xb[i + 1]));
+            am[1] = fmax3(am[1], fabsf(xb[i + 2]), fabsf(xb[i + 3]));
+          }
+          constexpr float kRcp6 = 0.16666667163372040f;  // 1/6 rounded to fp32
+          const uint32_t sb = f32_to_e4m3(div_step(fmaxf(am[0], am[1]), 6.0f, kRcp6));
+          const float sf = __half2float(__ushort_as_half(static_cast<uint16_t>(e4m3_to_f16x2_dup(sb))));
+          sw[blk >> 2] |= sb << ((blk & 3) * 8);
+          w[hb] = encode_block(xb, sf, sf > 0.f ? __frcp_rn(sf) : 0.f);
+          if (!(sf > 0.f)) w[hb] = make_uint2(0u, 0u);
+        }
+        *reinterpret_cast<uint4 *>(oc + sw64_off(r, c)) = make_uint4(w[0].x, w[0].y, w[1].x, w[1].y);
+      }
+      *reinterpret_cast<uint2 *>(sm.out_scales[b] + r * 8) = make_uint2(sw[0], sw[1]);
+
+      const int64_t row0 = (is_v ? t - tiles_per_tensor : t) * kRows;
+      const bool full_tile = row0 + kRows <= rows;
+      uint8_t *scales = is_v ? v_scales : k_scales;
+      if (!full_tile && row0 + r < rows)
+        *reinterpret_cast<uint2 *>(scales + (row0 + r) * 8) = make_uint2(sw[0], sw[1]);
+
+      fence_proxy_async_smem();
+      named_bar_sync(1, kRows);
+      if (tid == 0) {
+        // the tensor store clips rows past the end of the tensor
+        tma_store_2d(is_v ? &tm_v_out : &tm_k_out, 0, static_cast<int32_t>(row0), smem_u32(oc));
+        if (full_tile) bulk_s2g(scales + row0 * 8, smem_u32(&sm.out_scales[b][0]), kOutScaleBytes);
+        bulk_commit();
+      }
+    }
+    if (tid == 0) bulk_wait<0>();
+  }
+  __syncthreads();
+}
+
+}  // namespace
+
+cudaError_t launch_store_build_fp4(const CUtensorMap &k_in, const CUtensorMap &v_in, const CUtensorMap &k_out,
+                                   const CUtensorMap &v_out, uint8_t *k_scales, uint8_t *v_scales, int64_t rows,
+                                   int num_sms, uint32_t *err, uint64_t timeout_ns, cudaStream_t stream) {
+  static_assert(offsetof(Fp4BuildSmem, out_codes) % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
+  static_assert(kOutCodeBytes % 1024 == 0, "each code tile starts on a swizzle-atom boundary");
+  const int64_t tiles = (rows + kRows - 1) / kRows;
+  if (tiles == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(store_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kFp4BuildSmemBytes));
+  if (e != cudaSuccess) return e;
+  int64_t grid = static_cast<int64_t>(num_sms) * 2;
+  if (grid > 2 * tiles) grid = 2 * tiles;
+  store_fp4_kernel<<<static_cast<unsigned>(grid), kThreads, kFp4BuildSmemBytes, stream>>>(
+      k_in, v_in, k_out, v_out, k_scales, v_scales, rows, tiles, err, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace h3kv

@@ -21,8 +21,9 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported():
     names = declared_functions()
-    assert len(names) == 18
+    assert len(names) == 21
     assert {"h3kv_attend_f8", "h3kv_build_store_f8", "h3kv_f8_v_stride", "h3kv_store_f8_bytes"} <= set(names)
+    assert {"h3kv_attend_fp4", "h3kv_build_store_fp4", "h3kv_store_fp4_bytes"} <= set(names)
     lib = ctypes.CDLL(b.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -30,7 +31,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_abi_version_and_strings():
-    assert b.h3kv_abi_version() == 3
+    assert b.h3kv_abi_version() == 4
     for st in range(5):
         assert b.h3kv_strerror(st)
     assert b.h3kv_strerror(99) == b"unknown status"
@@ -180,3 +181,41 @@ def test_hostio_checks():
     assert hi(0, 256, ctypes.byref(st), 64, 0, 0.0, 4096, 4096, need, None) == b.H3KV_ERR_INVALID_ARG
     assert hi(4096, 256, ctypes.byref(st), 0, 0, 0.0, 4096, 4096, need, None) == b.H3KV_ERR_INVALID_ARG
     assert hi(4096, 0, ctypes.byref(st), 64, 0, 0.0, 4096, 4096, need, None) == b.H3KV_OK
+
+
+def test_store_fp4_sizes():
+    # 0.5625 byte per element: 64 code bytes and 8 scale bytes per 128 values
+    assert b.h3kv_store_fp4_bytes(32, 217088, 128) == 2 * 32 * 217088 * 72
+    assert b.h3kv_store_fp4_bytes(1, 77, 128) == 2 * 77 * 72
+    assert b.h3kv_store_fp4_bytes(1, 10, 64) == 0 and b.h3kv_store_fp4_bytes(-1, 10, 128) == 0
+
+
+def _store_fp4(heads=1, seq=256, ptr=4096, head_dim=128):
+    return b.h3kv_store_fp4(ptr, ptr, ptr, ptr, heads, seq, head_dim)
+
+
+def test_build_store_fp4_rejects_bad_arguments():
+    st = _store_fp4()
+    bs = b.h3kv_build_store_fp4
+    assert bs(4096, 4096, 1, 256, 128, None, None) == b.H3KV_ERR_INVALID_ARG
+    assert bs(4096, 4096, 1, 256, 64, ctypes.byref(st), None) == b.H3KV_ERR_UNSUPPORTED
+    assert bs(4096, 4096, 2, 256, 128, ctypes.byref(st), None) == b.H3KV_ERR_INVALID_ARG   # shape mismatch
+    assert bs(0, 4096, 1, 256, 128, ctypes.byref(st), None) == b.H3KV_ERR_INVALID_ARG      # null K
+    assert bs(4096, 4100, 1, 256, 128, ctypes.byref(st), None) == b.H3KV_ERR_INVALID_ARG   # misaligned V
+    assert bs(4096, 4096, 1, 256, 128, ctypes.byref(_store_fp4(ptr=0)), None) == b.H3KV_ERR_INVALID_ARG
+    big = _store_fp4(heads=1 << 20, seq=1 << 12)
+    assert bs(4096, 4096, 1 << 20, 1 << 12, 128, ctypes.byref(big), None) == b.H3KV_ERR_INVALID_ARG  # rows
+    assert bs(0, 0, 0, 0, 128, ctypes.byref(_store_fp4(heads=0, seq=0, ptr=0)), None) == b.H3KV_OK
+
+
+def test_attend_fp4_rejects_bad_arguments():
+    st = _store_fp4()
+    at = b.h3kv_attend_fp4
+    assert at(4096, 256, None, 256, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    assert at(4096, 256, ctypes.byref(st), 0, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG      # q_chunk 0
+    assert at(4096, 256, ctypes.byref(st), 64, 100, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG   # kv_block % 128
+    assert at(4096, 256, ctypes.byref(_store_fp4(head_dim=64)), 64, 0, 0.0, 4096, None) == b.H3KV_ERR_UNSUPPORTED
+    assert at(4104, 256, ctypes.byref(st), 64, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG     # misaligned Q
+    assert at(4096, 256, ctypes.byref(st), 64, 0, 0.0, 0, None) == b.H3KV_ERR_INVALID_ARG        # null O
+    assert at(4096, 256, ctypes.byref(_store_fp4(seq=0)), 64, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    assert at(4096, 0, ctypes.byref(st), 64, 0, 0.0, 4096, None) == b.H3KV_OK

@@ -41,7 +41,7 @@ def test_selftest_wait_runs_out_and_context_survives(cuda):
     _tiny_check(cuda)
 
 
-@pytest.mark.parametrize("path", ["store", "kvi8r", "exact", "store_f8", "kvf8s"])
+@pytest.mark.parametrize("path", ["store", "kvi8r", "exact", "store_f8", "kvf8s", "store_fp4", "kvfp4"])
 def test_kernels_give_up_under_tiny_wait_limit(cuda, path):
     b = _b()
     s = torch.cuda.current_stream().cuda_stream
@@ -49,6 +49,7 @@ def test_kernels_give_up_under_tiny_wait_limit(cuda, path):
     q, k, v = q.to(cuda), k.to(cuda), v.to(cuda)
     st = b.build_store(k, v)
     st8 = b.build_store_f8(k, v)
+    st4 = b.build_store_fp4(k, v)
     assert b.h3kv_sync_status(s) == b.H3KV_OK
     b.check(b.h3kv_set_wait_timeout_ns(1))
     try:
@@ -60,12 +61,16 @@ def test_kernels_give_up_under_tiny_wait_limit(cuda, path):
             b.attend_exact(q, k, v, q_chunk=4096, kv_block=0)
         elif path == "store_f8":
             b.build_store_f8(k, v, out=st8)
+        elif path == "store_fp4":
+            b.build_store_fp4(k, v, out=st4)
+        elif path == "kvfp4":
+            b.attend_fp4(q, st4, q_chunk=4096, kv_block=0)
         else:
             b.attend_f8(q, st8, q_chunk=4096, kv_block=0)
         status = b.h3kv_sync_status(s)
     finally:
         b.check(b.h3kv_set_wait_timeout_ns(0))
-    if path in ("store", "store_f8"):
+    if path in ("store", "store_f8", "store_fp4"):
         # the store builds' waits (bulk copies landing in shared memory)
         # usually end inside the first suspended try_wait, before the limit is
         # checked; either outcome is fine as long as the call ends and the
