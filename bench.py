@@ -38,6 +38,7 @@ from store_h3kv_build_gb300 import synth  # noqa: E402
 METRIC = "kvi8r attention TFLOP/s at 217k tokens (1 GB300) + store-build GB/s"
 UNIT = "TFLOP/s"
 HEAD_DIM = 128
+MUFU_EX2_PER_CLK_PER_SM = 32  # ex2 throughput measured on GB300 (a dependent-free MUFU loop)
 KERNEL_SOURCES = ["store_h3kv_build_gb300/csrc/attend.cuh", "store_h3kv_build_gb300/csrc/attend_kvi8r.cu",
                   "store_h3kv_build_gb300/csrc/ptx.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attend_kvi8r_traffic.json")
@@ -340,6 +341,16 @@ def run_ours(args, w, name):
     flops = attention_flops(H, L, L)
     value = job_throughput(world, flops * args.steps, total_ms / 1e3) / 1e12
 
+    # device memory the attention call takes beyond the caller's buffers: the
+    # library allocates none, measured as the free-memory change around a call
+    torch.cuda.synchronize(dev)
+    free0 = torch.cuda.mem_get_info(dev)[0]
+    b.attend(q, st, q_chunk=q_chunk, kv_block=kv_block, out=out)
+    free1 = torch.cuda.mem_get_info(dev)[0]
+    torch.cuda.synchronize(dev)
+    free2 = torch.cuda.mem_get_info(dev)[0]
+    attend_transient = max(0, free0 - min(free1, free2))
+
     # ---- end to end through the public API with host buffers, measured right
     # after the device-resident steps (same thermal state as `value`; the
     # comparison paths below run afterwards)
@@ -354,12 +365,11 @@ def run_ours(args, w, name):
     e2e_steps = max(1, min(args.steps, 3))
 
     def e2e_step():
-        # K and V in, the store built, then Q streamed in and O out one query
-        # chunk at a time (h3kv_attend_hostio overlaps those copies with the
-        # attention of neighbouring chunks)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        b.build_store(k, v, out=st)
+        # the store built straight from K and V in pinned host memory (the
+        # build kernel reads them over NVLink-C2C), then Q streamed in and O
+        # out one query chunk at a time (h3kv_attend_hostio overlaps those
+        # copies with the attention of neighbouring chunks)
+        b.build_store(hk, hv, out=st)
         b.attend_hostio(hq, st, q_chunk=q_chunk, kv_block=kv_block, out=ho, scratch=hostio_scratch)
 
     e2e_step()
@@ -467,6 +477,11 @@ def run_ours(args, w, name):
         achieved = flops * args.steps / (attend_sum / 1e3) / 1e12
         traffic = recorded_traffic(n_chunks)
         build_gbs = store_bytes(H, L) * args.steps / (build_sum / 1e3) / 1e9
+        sm_hz = (clocks.summary().get("sm_mhz") or 0) * 1e6
+        n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        exp_count = H * L * L  # one exp2 per score
+        exp_rate = exp_count * args.steps / (attend_sum / 1e3)
+        mufu_peak = MUFU_EX2_PER_CLK_PER_SM * n_sms * sm_hz if sm_hz else None
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -511,8 +526,18 @@ def run_ours(args, w, name):
                          "flops_per_step": flops},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps, "clocks": e2e_clocks.summary(),
-                    "api": "K, V copied in; h3kv_build_store; h3kv_attend_hostio (pinned host Q in, O out, "
-                           "per query chunk)"},
+                    "api": "h3kv_build_store reading pinned host K, V over NVLink-C2C; h3kv_attend_hostio "
+                           "(pinned host Q in, O out, per query chunk)"},
+            "exp": {"count_per_step": exp_count, "per_s": exp_rate, "unit": "exp2/s",
+                    "mufu_peak_per_s": mufu_peak, "frac": exp_rate / mufu_peak if mufu_peak else None,
+                    "peak_source": f"{MUFU_EX2_PER_CLK_PER_SM} ex2 per clock per SM (measured on GB300) x "
+                                   f"{n_sms} SMs x the median sampled SM clock"},
+            "memory": {"store_bytes": st.nbytes(), "kv_bf16_bytes": 2 * H * L * HEAD_DIM * 2,
+                       "attend_transient_bytes": attend_transient,
+                       "hostio_scratch_bytes": int(b.h3kv_hostio_scratch_bytes(H, q_chunk)),
+                       "note": "the library allocates no device memory: the store, O and any scratch are "
+                               "caller-owned; attend_transient_bytes is the measured free-memory change "
+                               "around one call"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks.summary(),
             "wall_s_timed": t_wall,

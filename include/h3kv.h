@@ -93,7 +93,10 @@ size_t h3kv_store_bytes(int32_t heads, int64_t seq, int32_t head_dim);
  * the H3 Streamed Blocks Inputs table: rotate by the fixed Hadamard basis,
  * one fp16 absmax scale per token per head, int8 codes).  `out` describes the
  * destination buffers and must match heads/seq/head_dim.  K and V are read
- * once; codes and scales are written once. */
+ * once; codes and scales are written once.  K and V may be device memory or
+ * pinned host memory that the GPU addresses (on a Grace-Blackwell node the
+ * kernel reads them over NVLink-C2C), so the caller's K/V need never be
+ * copied into HBM; the store is the same bit for bit. */
 h3kv_status h3kv_build_store(const uint16_t *K, const uint16_t *V, int32_t heads, int64_t seq,
                              int32_t head_dim, const h3kv_store *out, void *stream);
 

@@ -38,3 +38,17 @@ def test_host_store_matches_device_store(cuda, heads, seq, q_chunk, kv_block):
     b.sync_status()
     assert torch.equal(o_dev, o_host)
     compare_attention(o_host, oracle.attend(q, oracle.build_store(k, v)), f"host store {heads}x{seq}")
+
+
+@pytest.mark.parametrize("heads,seq,group", [(2, 3000, 0), (1, 129, 0), (3, 1000, 32)])
+def test_store_built_from_host_inputs(cuda, heads, seq, group):
+    # bf16 K and V left in pinned host memory: the build kernel reads them
+    # over NVLink-C2C and writes the same store as from HBM copies
+    b = _b()
+    _, k, v = synth.make_qkv(heads, seq, seed=23, k_outliers=True)
+    hk, hv = k.pin_memory(), v.pin_memory()
+    dev = b.build_store(k.to(cuda), v.to(cuda), scale_group=group)
+    from_host = b.build_store(hk, hv, out=b.Store.empty(heads, seq, cuda, scale_group=group))
+    b.sync_status()
+    for name in ("k_codes", "v_codes", "k_scales", "v_scales"):
+        assert torch.equal(getattr(from_host, name), getattr(dev, name)), name
