@@ -123,18 +123,6 @@ bool encode_3d_u8(CUtensorMap *m, const void *base, uint64_t inner, uint64_t mid
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D map over kvfp4 codes [rows, 64 bytes]: box 64 x 128 rows with the
-// 64-byte swizzle (the store build's staging layout).
-bool encode_codes_fp4(CUtensorMap *m, const void *base, uint64_t rows) {
-  const cuuint64_t dims[2] = {64, rows};
-  const cuuint64_t strides[1] = {64};
-  const cuuint32_t box[2] = {64, 128};
-  const cuuint32_t es[2] = {1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // TMA coordinates are signed 32-bit; keep every row index below 2^31.
 constexpr int64_t kMaxRows = (1ll << 31) - 256;
 
@@ -197,13 +185,11 @@ h3kv_status h3kv_build_store(const uint16_t *K, const uint16_t *V, int32_t heads
   DeviceInfo *d = nullptr;
   h3kv_status st = device_info(&d);
   if (st != H3KV_OK) return st;
-  CUtensorMap k_in, v_in, k_out, v_out;
+  CUtensorMap k_in, v_in;
   if (!encode_2d(&k_in, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, rows, 2, 64) ||
-      !encode_2d(&v_in, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, 2, 64) ||
-      !encode_2d(&k_out, CU_TENSOR_MAP_DATA_TYPE_UINT8, out->k_codes, rows, 1, 128) ||
-      !encode_2d(&v_out, CU_TENSOR_MAP_DATA_TYPE_UINT8, out->v_codes, rows, 1, 128))
+      !encode_2d(&v_in, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, 2, 64))
     return H3KV_ERR_CUDA;
-  const cudaError_t e = h3kv::launch_store_build(k_in, v_in, k_out, v_out, out->k_scales, out->v_scales, rows,
+  const cudaError_t e = h3kv::launch_store_build(k_in, v_in, out->k_codes, out->v_codes, out->k_scales, out->v_scales, rows,
                                                  d->num_sms, groups, d->err, g_timeout_ns.load(),
                                                  static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? H3KV_OK : H3KV_ERR_CUDA;
@@ -578,12 +564,12 @@ h3kv_status h3kv_build_store_fp4(const uint16_t *K, const uint16_t *V, int32_t h
   DeviceInfo *d = nullptr;
   h3kv_status st = device_info(&d);
   if (st != H3KV_OK) return st;
-  CUtensorMap k_in, v_in, k_out, v_out;
+  CUtensorMap k_in, v_in;
   if (!encode_2d(&k_in, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, rows, 2, 64) ||
-      !encode_2d(&v_in, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, 2, 64) ||
-      !encode_codes_fp4(&k_out, out->k_codes, rows) || !encode_codes_fp4(&v_out, out->v_codes, rows))
+      !encode_2d(&v_in, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, 2, 64))
     return H3KV_ERR_CUDA;
-  const cudaError_t e = h3kv::launch_store_build_fp4(k_in, v_in, k_out, v_out, out->k_scales, out->v_scales, rows,
+  const cudaError_t e = h3kv::launch_store_build_fp4(k_in, v_in, out->k_codes, out->v_codes, out->k_scales,
+                                                     out->v_scales, rows,
                                                      d->num_sms, d->err, g_timeout_ns.load(),
                                                      static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? H3KV_OK : H3KV_ERR_CUDA;

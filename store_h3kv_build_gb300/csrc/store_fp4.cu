@@ -6,11 +6,10 @@
 // codes e2m1(x / s), all zero where s == 0.
 //
 // GB300 design: the HBM-bound stream of the kvi8r build.  A persistent grid
-// walks 128-row tiles (K tiles, then V tiles); one producer warp streams bf16
-// tiles into a 2-stage ring with TMA (128-byte swizzle), four compute warps
-// own one row per thread and write codes into a 64-byte-swizzled tile (16-byte
-// stores conflict free) that one thread stores with a TMA tensor store, and
-// the scales with one bulk copy.
+// (two CTAs per SM) walks 128-row tiles (K tiles, then V tiles); one producer
+// warp streams bf16 tiles into a 3-stage ring with TMA (128-byte swizzle), and
+// four compute warps own one row per thread and store its 64 code bytes and 8
+// scale bytes straight from registers.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -18,16 +17,12 @@ namespace h3kv {
 namespace {
 
 constexpr int kRows = 128;                  // rows per tile = compute threads
-constexpr int kStages = 2;                  // input ring depth (2 CTAs per SM)
+constexpr int kStages = 3;                  // input ring depth (2 CTAs per SM)
 constexpr int kInTileBytes = kRows * 256;   // bf16 [128 x 128]
-constexpr int kOutCodeBytes = kRows * 64;   // e2m1 pairs [128 x 64 bytes]
-constexpr int kOutScaleBytes = kRows * 8;   // e4m3 [128 x 8]
 constexpr int kThreads = kRows + 32;        // 4 compute warps + 1 producer warp
 
 struct Fp4BuildSmem {
   uint8_t in[kStages][kInTileBytes];
-  uint8_t out_codes[2][kOutCodeBytes];
-  uint8_t out_scales[2][kOutScaleBytes];
   uint64_t full[kStages];
   uint64_t empty[kStages];
   int abort;
@@ -35,24 +30,29 @@ struct Fp4BuildSmem {
 
 constexpr size_t kFp4BuildSmemBytes = sizeof(Fp4BuildSmem) + 1024;
 
-// Byte offset of 16-byte chunk c (0..3) of row r in a 64-byte-wide tile
-// stored with the 64-byte swizzle (chunk c sits at c ^ ((r / 2) mod 4)).
-__device__ __forceinline__ uint32_t sw64_off(uint32_t r, uint32_t c) { return r * 64u + ((c ^ ((r >> 1) & 3u)) << 4); }
-
-// x / d given r = 1/d rounded to fp32: q0 = x r corrected once by its exact
+// x / d given r ~ 1/d (within 2 ulp): q0 = x r corrected once by its exact
 // residual (Markstein's division step: e = q0 d - x by one fma, then
-// q0 - e r).  A quotient that is exactly representable -- the only kind that
-// can sit on a rounding midpoint of e2m1 or e4m3 here -- comes out exact, so
-// the nearest-even decision that follows is the one for x / d itself; a zero
-// keeps its sign.
+// q0 - e r).  For an exactly representable quotient t, q0 is within a few
+// ulp of t, the residual e is exact, and q0 - e r = t - (q0 - t)(r d - 1)
+// rounds to t; such quotients -- the only kind that can sit on a rounding
+// midpoint of e2m1 or e4m3 here -- come out exact, so the nearest-even
+// decision that follows is the one for x / d itself.  A zero keeps its sign.
 __device__ __forceinline__ float div_step(float x, float d, float r) {
   const float q0 = x * r;
   const float e = fmaf(q0, d, -x);
   return fmaf(e, -r, q0);
 }
 
-// Codes of one 16-value block x[0..15] with scale s > 0 (r = 1/s rounded to
-// fp32): e2m1 of x / s.  Returns the 16 nibbles in two words, element 0
+// Reciprocal to within one ulp (the hardware approximation); s here is a
+// normal fp32 number (an e4m3 scale, at least 2^-9).
+__device__ __forceinline__ float rcp_approx(float s) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+  return r;
+}
+
+// Codes of one 16-value block x[0..15] with scale s > 0 (r ~ 1/s): e2m1 of
+// x / s.  Returns the 16 nibbles in two words, element 0
 // lowest.
 __device__ __forceinline__ uint2 encode_block(const float *x, float s, float r) {
   float q[16];
@@ -66,7 +66,7 @@ __device__ __forceinline__ uint2 encode_block(const float *x, float s, float r) 
 
 __global__ void __launch_bounds__(kThreads, 2)
     store_fp4_kernel(const __grid_constant__ CUtensorMap tm_k_in, const __grid_constant__ CUtensorMap tm_v_in,
-                     const __grid_constant__ CUtensorMap tm_k_out, const __grid_constant__ CUtensorMap tm_v_out,
+                     uint8_t *__restrict__ k_codes, uint8_t *__restrict__ v_codes,
                      uint8_t *__restrict__ k_scales, uint8_t *__restrict__ v_scales, int64_t rows,
                      int64_t tiles_per_tensor, uint32_t *err, uint64_t timeout_ns) {
   extern __shared__ uint8_t smem_raw[];
@@ -121,9 +121,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
       const int s = it % kStages;
       const uint32_t ph = (it / kStages) & 1;
-      const int b = it & 1;
-      // output tile b must no longer be read by the stores of tile it-2
-      if (tid == 0) bulk_wait_read<1>();
       const bool ok = mbar_wait(smem_u32(&sm.full[s]), ph, wctx);
       if (!named_bar_and(1, kRows, ok)) break;
 
@@ -160,7 +157,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
 
-      uint8_t *oc = sm.out_codes[b];
+      const int64_t row0 = (is_v ? t - tiles_per_tensor : t) * kRows;
+      const bool row_ok = row0 + r < rows;
+      uint8_t *oc = (is_v ? v_codes : k_codes) + (row_ok ? row0 + r : 0) * 64;
       uint32_t sw[2] = {0u, 0u};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -180,40 +179,23 @@ __global__ void __launch_bounds__(kThreads, 2)
           const uint32_t sb = f32_to_e4m3(div_step(fmaxf(am[0], am[1]), 6.0f, kRcp6));
           const float sf = __half2float(__ushort_as_half(static_cast<uint16_t>(e4m3_to_f16x2_dup(sb))));
           sw[blk >> 2] |= sb << ((blk & 3) * 8);
-          w[hb] = encode_block(xb, sf, sf > 0.f ? __frcp_rn(sf) : 0.f);
+          w[hb] = encode_block(xb, sf, sf > 0.f ? rcp_approx(sf) : 0.f);
           if (!(sf > 0.f)) w[hb] = make_uint2(0u, 0u);
         }
-        *reinterpret_cast<uint4 *>(oc + sw64_off(r, c)) = make_uint4(w[0].x, w[0].y, w[1].x, w[1].y);
+        if (row_ok) *reinterpret_cast<uint4 *>(oc + c * 16) = make_uint4(w[0].x, w[0].y, w[1].x, w[1].y);
       }
-      *reinterpret_cast<uint2 *>(sm.out_scales[b] + r * 8) = make_uint2(sw[0], sw[1]);
-
-      const int64_t row0 = (is_v ? t - tiles_per_tensor : t) * kRows;
-      const bool full_tile = row0 + kRows <= rows;
       uint8_t *scales = is_v ? v_scales : k_scales;
-      if (!full_tile && row0 + r < rows)
-        *reinterpret_cast<uint2 *>(scales + (row0 + r) * 8) = make_uint2(sw[0], sw[1]);
-
-      fence_proxy_async_smem();
-      named_bar_sync(1, kRows);
-      if (tid == 0) {
-        // the tensor store clips rows past the end of the tensor
-        tma_store_2d(is_v ? &tm_v_out : &tm_k_out, 0, static_cast<int32_t>(row0), smem_u32(oc));
-        if (full_tile) bulk_s2g(scales + row0 * 8, smem_u32(&sm.out_scales[b][0]), kOutScaleBytes);
-        bulk_commit();
-      }
+      if (row_ok) *reinterpret_cast<uint2 *>(scales + (row0 + r) * 8) = make_uint2(sw[0], sw[1]);
     }
-    if (tid == 0) bulk_wait<0>();
   }
   __syncthreads();
 }
 
 }  // namespace
 
-cudaError_t launch_store_build_fp4(const CUtensorMap &k_in, const CUtensorMap &v_in, const CUtensorMap &k_out,
-                                   const CUtensorMap &v_out, uint8_t *k_scales, uint8_t *v_scales, int64_t rows,
+cudaError_t launch_store_build_fp4(const CUtensorMap &k_in, const CUtensorMap &v_in, uint8_t *k_out,
+                                   uint8_t *v_out, uint8_t *k_scales, uint8_t *v_scales, int64_t rows,
                                    int num_sms, uint32_t *err, uint64_t timeout_ns, cudaStream_t stream) {
-  static_assert(offsetof(Fp4BuildSmem, out_codes) % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
-  static_assert(kOutCodeBytes % 1024 == 0, "each code tile starts on a swizzle-atom boundary");
   const int64_t tiles = (rows + kRows - 1) / kRows;
   if (tiles == 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(store_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
