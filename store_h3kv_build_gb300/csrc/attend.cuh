@@ -113,6 +113,35 @@ __device__ __forceinline__ uint32_t dq_granule(int lane) {
   return (lane & 3) + 4 * (hf ^ (q4 & 1));
 }
 
+// Shared-memory byte offsets of one lane's dequantisation work inside a K/V
+// tile, computed once per kernel.  The lane's row in iteration `it` is
+// dw*32 + 4*it + rr (rr = 2*(q4/2) + hf, below 4), so every address is a
+// per-lane base plus it*512 bytes (a compile-time immediate once the loop is
+// unrolled); in the 128-byte swizzle the row's low three bits alternate
+// between rr and rr + 4, which flips bit 6 of the granule offset on odd
+// iterations.
+struct DqOffsets {
+  uint32_t ld8;       // int8 codes of iteration 0 (second half of the tile); + it*512
+  uint32_t ld4;       // kvfp4 codes of iteration 0 (start of the tile); + it*256
+  uint32_t st[2][2];  // fp16 granules G0, G0 + 1 for even / odd iterations; + it*512
+};
+__device__ __forceinline__ DqOffsets dq_offsets(int dw, int lane) {
+  const uint32_t g = dq_granule(lane);
+  const uint32_t rr = 2u * (static_cast<uint32_t>(lane) >> 4) + ((static_cast<uint32_t>(lane) >> 2) & 1u);
+  const uint32_t row0 = static_cast<uint32_t>(dw) * 32u + rr;
+  const uint32_t base = (g >> 2) * kChunkBytes + row0 * 128u;
+  const uint32_t G0 = (g & 3u) * 2u;
+  const uint32_t a0 = (G0 ^ rr) << 4, a1 = ((G0 + 1u) ^ rr) << 4;
+  DqOffsets o;
+  o.ld8 = kChunkBytes + row0 * 128u + g * 16u;
+  o.ld4 = row0 * 64u + g * 8u;
+  o.st[0][0] = base + a0;
+  o.st[0][1] = base + a1;
+  o.st[1][0] = base + (a0 ^ 64u);
+  o.st[1][1] = base + (a1 ^ 64u);
+  return o;
+}
+
 // Scales of the rows this lane dequantises (rows past `valid` get 0).  With
 // kGroups = 4 a row has one scale per 32 values and the lane's 16-value
 // granule g takes scale g / 2 of its row.
@@ -135,19 +164,16 @@ __device__ __forceinline__ void dequant_scales(const uint16_t *scales, int valid
 // 128-byte slot with row r's fp16 columns 64-127, and every row is read by
 // one load instruction of its warp before any lane writes it, so in place is
 // safe.
-__device__ __forceinline__ void dequant_tile(uint8_t *tile, const uint16_t (&sc)[8], int dw, int lane) {
-  const uint32_t g = dq_granule(lane);
+__device__ __forceinline__ void dequant_tile(uint8_t *tile, const uint16_t (&sc)[8], const DqOffsets &off) {
 #pragma unroll
   for (int it = 0; it < 8; ++it) {
-    const uint32_t r = dq_row(dw, it, lane);
-    const uint4 raw = *reinterpret_cast<const uint4 *>(tile + kChunkBytes + r * 128 + g * 16);
+    const uint4 raw = *reinterpret_cast<const uint4 *>(tile + off.ld8 + it * 512);
     const __half s = __ushort_as_half(sc[it]);
     uint32_t o[8];
     dequant16(raw, __halves2half2(s, s), o);
-    uint8_t *half_base = tile + (g >> 2) * kChunkBytes;
-    const uint32_t G0 = (g & 3) * 2;
-    *reinterpret_cast<uint4 *>(half_base + sw128_off(r, G0)) = make_uint4(o[0], o[1], o[2], o[3]);
-    *reinterpret_cast<uint4 *>(half_base + sw128_off(r, G0 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+    uint8_t *row = tile + it * 512;
+    *reinterpret_cast<uint4 *>(row + off.st[it & 1][0]) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4 *>(row + off.st[it & 1][1]) = make_uint4(o[4], o[5], o[6], o[7]);
   }
 }
 
@@ -190,24 +216,21 @@ __device__ __forceinline__ void dequant_scales_fp4(const uint8_t *scales, int va
 // waits' outcomes: every warp reaches it whether or not its wait succeeded),
 // and only then does any thread write.  Returns false, having written
 // nothing, when some warp's wait ran out.  Output layout as dequant_tile.
-__device__ __forceinline__ bool dequant_tile_fp4(uint8_t *tile, bool loaded, const uint32_t (&sc)[2], int dw,
-                                                 int lane) {
-  const uint32_t g = dq_granule(lane);
+__device__ __forceinline__ bool dequant_tile_fp4(uint8_t *tile, bool loaded, const uint32_t (&sc)[2],
+                                                 const DqOffsets &off) {
   uint2 raw[8];
 #pragma unroll
   for (int it = 0; it < 8; ++it)
-    raw[it] = loaded ? *reinterpret_cast<const uint2 *>(tile + dq_row(dw, it, lane) * 64 + g * 8) : make_uint2(0u, 0u);
+    raw[it] = loaded ? *reinterpret_cast<const uint2 *>(tile + off.ld4 + it * 256) : make_uint2(0u, 0u);
   if (!named_bar_and(1, 128, loaded)) return false;
 #pragma unroll
   for (int it = 0; it < 8; ++it) {
-    const uint32_t r = dq_row(dw, it, lane);
     uint32_t o[8];
     // the iteration's scale byte twice: the fp16 pair (s, s)
     dequant16_fp4(raw[it], e4m3x2_to_f16x2(__byte_perm(sc[it >> 2], 0u, (it & 3) * 0x11u)), o);
-    uint8_t *half_base = tile + (g >> 2) * kChunkBytes;
-    const uint32_t G0 = (g & 3) * 2;
-    *reinterpret_cast<uint4 *>(half_base + sw128_off(r, G0)) = make_uint4(o[0], o[1], o[2], o[3]);
-    *reinterpret_cast<uint4 *>(half_base + sw128_off(r, G0 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+    uint8_t *row = tile + it * 512;
+    *reinterpret_cast<uint4 *>(row + off.st[it & 1][0]) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4 *>(row + off.st[it & 1][1]) = make_uint4(o[4], o[5], o[6], o[7]);
   }
   return true;
 }
@@ -546,18 +569,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t *ksc = a.k_fp4_scales + static_cast<int64_t>(h) * a.kv_stride * 8;
       const uint8_t *vsc = a.v_fp4_scales + static_cast<int64_t>(h) * a.kv_stride * 8;
       uint32_t sck[2], scv[2];
+      const DqOffsets off = dq_offsets(dw, lane);
       for (int j = 0; j < n_tiles; ++j) {
         const int64_t tok0 = static_cast<int64_t>(j) * kBN;
         const int valid = static_cast<int>(a.kv_seq - tok0 < kBN ? a.kv_seq - tok0 : kBN);
         const int ks = j % kNK, vs = j % kNV;
         dequant_scales_fp4(ksc + tok0 * 8, valid, dw, lane, sck);
         dequant_scales_fp4(vsc + tok0 * 8, valid, dw, lane, scv);
-        if (!dequant_tile_fp4(sm.k[ks], warp_wait(smem_u32(&sm.k_load[ks]), (j / kNK) & 1, wctx), sck, dw, lane))
+        if (!dequant_tile_fp4(sm.k[ks], warp_wait(smem_u32(&sm.k_load[ks]), (j / kNK) & 1, wctx), sck, off))
           break;
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sm.k_ready[ks]));
-        if (!dequant_tile_fp4(sm.v[vs], warp_wait(smem_u32(&sm.v_load[vs]), (j / kNV) & 1, wctx), scv, dw, lane))
+        if (!dequant_tile_fp4(sm.v[vs], warp_wait(smem_u32(&sm.v_load[vs]), (j / kNV) & 1, wctx), scv, off))
           break;
         fence_proxy_async_smem();
         __syncwarp();
@@ -568,6 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint16_t *ksc = a.k_scales + static_cast<int64_t>(h) * a.kv_stride * kGroups;
       const uint16_t *vsc = a.v_scales + static_cast<int64_t>(h) * a.kv_stride * kGroups;
       uint16_t sck[8], scv[8];
+      const DqOffsets off = dq_offsets(dw, lane);
       for (int j = 0; j < n_tiles; ++j) {
         const int64_t tok0 = static_cast<int64_t>(j) * kBN;
         const int valid = static_cast<int>(a.kv_seq - tok0 < kBN ? a.kv_seq - tok0 : kBN);
@@ -576,12 +601,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         dequant_scales<kGroups>(ksc + tok0 * kGroups, valid, dw, lane, sck);
         dequant_scales<kGroups>(vsc + tok0 * kGroups, valid, dw, lane, scv);
         if (!warp_wait(smem_u32(&sm.k_load[ks]), (j / kNK) & 1, wctx)) break;
-        dequant_tile(sm.k[ks], sck, dw, lane);
+        dequant_tile(sm.k[ks], sck, off);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sm.k_ready[ks]));
         if (!warp_wait(smem_u32(&sm.v_load[vs]), (j / kNV) & 1, wctx)) break;
-        dequant_tile(sm.v[vs], scv, dw, lane);
+        dequant_tile(sm.v[vs], scv, off);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sm.v_ready[vs]));
