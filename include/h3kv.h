@@ -28,6 +28,8 @@
  *  - Empty work (heads == 0 or a zero sequence length) returns H3KV_OK and
  *    launches nothing, except that attending a non-empty query set to an
  *    empty key set is H3KV_ERR_INVALID_ARG (the softmax has no terms).
+ *  - Attention entry points take at most 65535 heads (one grid row per
+ *    head); more is H3KV_ERR_INVALID_ARG.
  */
 #ifndef H3KV_H
 #define H3KV_H

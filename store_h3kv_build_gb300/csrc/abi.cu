@@ -126,6 +126,9 @@ bool encode_3d_u8(CUtensorMap *m, const void *base, uint64_t inner, uint64_t mid
 // TMA coordinates are signed 32-bit; keep every row index below 2^31.
 constexpr int64_t kMaxRows = (1ll << 31) - 256;
 
+// The attention kernels run one grid row per head (grid.y <= 65535).
+constexpr int32_t kMaxHeads = 65535;
+
 h3kv_status check_chunks(int32_t q_chunk, int32_t kv_block) {
   if (q_chunk < 1) return H3KV_ERR_INVALID_ARG;
   if (kv_block < 0 || kv_block % H3KV_KV_TILE != 0) return H3KV_ERR_INVALID_ARG;
@@ -204,7 +207,7 @@ h3kv_status h3kv_attend(const uint16_t *Q, int64_t q_seq, const h3kv_store *stor
   const int groups = scale_groups_of(store);
   if (groups == 0) return H3KV_ERR_INVALID_ARG;
   if (store->heads == 0 || q_seq == 0) return H3KV_OK;
-  if (store->seq == 0) return H3KV_ERR_INVALID_ARG;
+  if (store->seq == 0 || store->heads > kMaxHeads) return H3KV_ERR_INVALID_ARG;
   if (static_cast<int64_t>(store->heads) * q_seq > kMaxRows || static_cast<int64_t>(store->heads) * store->seq > kMaxRows)
     return H3KV_ERR_INVALID_ARG;
   if (!Q || !O || !store->k_codes || !store->v_codes || !store->k_scales || !store->v_scales)
@@ -249,7 +252,7 @@ h3kv_status h3kv_attend_exact(const uint16_t *Q, int64_t q_seq, const uint16_t *
   h3kv_status st = check_chunks(q_chunk, kv_block);
   if (st != H3KV_OK) return st;
   if (heads == 0 || q_seq == 0) return H3KV_OK;
-  if (kv_seq == 0) return H3KV_ERR_INVALID_ARG;
+  if (kv_seq == 0 || heads > kMaxHeads) return H3KV_ERR_INVALID_ARG;
   if (static_cast<int64_t>(heads) * q_seq > kMaxRows || static_cast<int64_t>(heads) * kv_seq > kMaxRows)
     return H3KV_ERR_INVALID_ARG;
   if (!Q || !K || !V || !O) return H3KV_ERR_INVALID_ARG;
@@ -300,7 +303,7 @@ h3kv_status h3kv_attend_staged(const uint16_t *Q, int64_t q_seq, const h3kv_stor
   if (scale_groups_of(store) == 0) return H3KV_ERR_INVALID_ARG;
   if (scale_groups_of(store) != 1) return H3KV_ERR_UNSUPPORTED;
   if (store->heads == 0 || q_seq == 0) return H3KV_OK;
-  if (store->seq == 0) return H3KV_ERR_INVALID_ARG;
+  if (store->seq == 0 || store->heads > kMaxHeads) return H3KV_ERR_INVALID_ARG;
   const int64_t H = store->heads;
   if (H * q_seq > kMaxRows || H * store->seq > kMaxRows) return H3KV_ERR_INVALID_ARG;
   if (!Q || !O || !staging || !state || !store->k_codes || !store->v_codes || !store->k_scales ||
@@ -376,7 +379,7 @@ h3kv_status h3kv_attend_hostio(const uint16_t *Q_host, int64_t q_seq, const h3kv
   const int groups = scale_groups_of(store);
   if (groups == 0) return H3KV_ERR_INVALID_ARG;
   if (store->heads == 0 || q_seq == 0) return H3KV_OK;
-  if (store->seq == 0) return H3KV_ERR_INVALID_ARG;
+  if (store->seq == 0 || store->heads > kMaxHeads) return H3KV_ERR_INVALID_ARG;
   const int64_t H = store->heads;
   if (H * q_seq > kMaxRows || H * store->seq > kMaxRows) return H3KV_ERR_INVALID_ARG;
   if (!Q_host || !O_host || !scratch || !store->k_codes || !store->v_codes || !store->k_scales ||
@@ -504,7 +507,7 @@ h3kv_status h3kv_attend_f8(const uint16_t *Q, int64_t q_seq, const h3kv_store_f8
   h3kv_status st = check_chunks(q_chunk, kv_block);
   if (st != H3KV_OK) return st;
   if (store->heads == 0 || q_seq == 0) return H3KV_OK;
-  if (store->seq == 0 || store->heads > 65535) return H3KV_ERR_INVALID_ARG;
+  if (store->seq == 0 || store->heads > kMaxHeads) return H3KV_ERR_INVALID_ARG;
   const int64_t H = store->heads;
   if (H * q_seq > kMaxRows || H * store->seq > kMaxRows) return H3KV_ERR_INVALID_ARG;
   if (!Q || !O || !store->k_codes || !store->v_codes_t || !store->k_scales || !store->v_scales)
@@ -582,7 +585,7 @@ h3kv_status h3kv_attend_fp4(const uint16_t *Q, int64_t q_seq, const h3kv_store_f
   h3kv_status st = check_chunks(q_chunk, kv_block);
   if (st != H3KV_OK) return st;
   if (store->heads == 0 || q_seq == 0) return H3KV_OK;
-  if (store->seq == 0) return H3KV_ERR_INVALID_ARG;
+  if (store->seq == 0 || store->heads > kMaxHeads) return H3KV_ERR_INVALID_ARG;
   if (static_cast<int64_t>(store->heads) * q_seq > kMaxRows || static_cast<int64_t>(store->heads) * store->seq > kMaxRows)
     return H3KV_ERR_INVALID_ARG;
   if (!Q || !O || !store->k_codes || !store->v_codes || !store->k_scales || !store->v_scales)

@@ -219,3 +219,22 @@ def test_attend_fp4_rejects_bad_arguments():
     assert at(4096, 256, ctypes.byref(st), 64, 0, 0.0, 0, None) == b.H3KV_ERR_INVALID_ARG        # null O
     assert at(4096, 256, ctypes.byref(_store_fp4(seq=0)), 64, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
     assert at(4096, 0, ctypes.byref(st), 64, 0, 0.0, 4096, None) == b.H3KV_OK
+
+
+def test_attention_rejects_more_than_65535_heads():
+    # one grid row per head: more heads than a grid dimension holds is an
+    # argument error on the host, not a failed launch
+    H = 65536
+    st = b.h3kv_store(4096, 4096, 4096, 4096, H, 16, 128, 0)
+    assert b.h3kv_attend(4096, 16, ctypes.byref(st), 16, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    assert b.h3kv_attend_exact(4096, 16, 4096, 4096, H, 16, 128, 16, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    big = b.h3kv_staging_bytes(H, 128)
+    assert b.h3kv_attend_staged(4096, 16, ctypes.byref(st), 16, 128, 0.0, 4096, 4096, big, 4096,
+                                None) == b.H3KV_ERR_INVALID_ARG
+    need = b.h3kv_hostio_scratch_bytes(H, 16)
+    assert b.h3kv_attend_hostio(4096, 16, ctypes.byref(st), 16, 0, 0.0, 4096, 4096, need,
+                                None) == b.H3KV_ERR_INVALID_ARG
+    st4 = b.h3kv_store_fp4(4096, 4096, 4096, 4096, H, 16, 128)
+    assert b.h3kv_attend_fp4(4096, 16, ctypes.byref(st4), 16, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
+    st8 = b.h3kv_store_f8(4096, 4096, 4096, 4096, 4096, H, 16, 128)
+    assert b.h3kv_attend_f8(4096, 16, ctypes.byref(st8), 16, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
