@@ -283,3 +283,36 @@ def test_fp4_scale_codes_are_e4m3(cuda):
     for s in (st.k_scales, st.v_scales):
         d = f8.e4m3_decode(s.cpu().numpy())
         assert np.isfinite(d).all() and (d >= 0).all()
+
+
+def test_attend_fp4_query_outliers_and_zero_keys(cuda):
+    # query rows 100x larger than the rest (a much sharper softmax), and a
+    # second head whose keys are all zero: every score is 0, so the output
+    # is the mean of the dequantised V rows
+    b = _b()
+    q, k, v = synth.make_qkv(2, 900, seed=22)
+    q = q.float()
+    q[:, ::7] *= 100
+    q = q.to(torch.bfloat16)
+    k = k.clone()
+    k[1] = 0
+    st = _build(k.to(cuda), v.to(cuda))
+    out = b.attend_fp4(q.to(cuda), st, q_chunk=300, kv_block=256)
+    b.sync_status()
+    g = gpu_store_numpy(st)
+    assert not g["k_scales"][1].any()
+    compare_fp4_attention(out, q, g, "q outliers / zero keys")
+    mean_v = f4.dequant(g["v_codes"][1], g["v_scales"][1]).mean(axis=0)
+    assert np.max(np.abs(out[1].cpu().double().numpy() - mean_v[None, :])) < 1e-4
+
+
+def test_attend_fp4_every_kv_block(cuda):
+    # the log-sum-exp combine over every kv_block from one tile to one block
+    b = _b()
+    q, k, v = synth.make_qkv(1, 1000, seed=24, q_seq=300, k_outliers=True)
+    st = _build(k.to(cuda), v.to(cuda))
+    g = gpu_store_numpy(st)
+    for kvb in (128, 256, 384, 512, 1024, 0):
+        out = b.attend_fp4(q.to(cuda), st, q_chunk=128, kv_block=kvb)
+        b.sync_status()
+        compare_fp4_attention(out, q, g, f"kv_block={kvb}")
