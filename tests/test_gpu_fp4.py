@@ -22,6 +22,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from oracle import kvf8s as f8
 from oracle import kvfp4 as f4
 from store_h3kv_build_gb300 import synth
@@ -288,7 +289,10 @@ def test_fp4_scale_codes_are_e4m3(cuda):
 def test_attend_fp4_query_outliers_and_zero_keys(cuda):
     # query rows 100x larger than the rest (a much sharper softmax), and a
     # second head whose keys are all zero: every score is 0, so the output
-    # is the mean of the dequantised V rows
+    # is the mean of the dequantised V rows.  With scores of order 100 the
+    # kernel's fp16 query (its stated precision step, 2^-11 relative) moves
+    # logits by tenths, so the reference takes the rotated query rounded to
+    # fp16 as well; the rest (fp16 weights, fp32 sums) stays within the bar
     b = _b()
     q, k, v = synth.make_qkv(2, 900, seed=22)
     q = q.float()
@@ -301,7 +305,11 @@ def test_attend_fp4_query_outliers_and_zero_keys(cuda):
     b.sync_status()
     g = gpu_store_numpy(st)
     assert not g["k_scales"][1].any()
-    compare_fp4_attention(out, q, g, "q outliers / zero keys")
+    q16 = oracle.fp16_round(oracle.rotate(q))
+    ref = np.stack([oracle.softmax_attention(q16[h], f4.dequant(g["k_codes"][h], g["k_scales"][h]),
+                                             f4.dequant(g["v_codes"][h], g["v_scales"][h]), 1 / np.sqrt(128))
+                    for h in range(2)])
+    compare_attention(out, ref, "q outliers / zero keys")
     mean_v = f4.dequant(g["v_codes"][1], g["v_scales"][1]).mean(axis=0)
     assert np.max(np.abs(out[1].cpu().double().numpy() - mean_v[None, :])) < 1e-4
 
