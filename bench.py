@@ -545,7 +545,11 @@ def run_ours(args, w, name):
         if not args.no_cpu_baseline:
             att, gbs, s, desc = time_oracle_sample(w, rows=args.ref_rows)
             line["cpu_baseline"] = {"value": att, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-                                    "sample": desc, "store_gbs": gbs, "seconds": s}
+                                    "sample": desc, "store_gbs": gbs, "seconds": s,
+                                    "os_cpu_count": os.cpu_count(),
+                                    "full_call_s_extrapolated": flops / (att * 1e12) + store_bytes(H, L) / (gbs * 1e9),
+                                    "extrapolation": "the whole workload's attention FLOPs at the sample's FLOP/s "
+                                                     "plus its store bytes at the sample's GB/s (not measured)"}
             att8, gbs8, s8, desc8 = time_oracle_sample_f8(w)
             line["f8_store"]["cpu_baseline"] = {"value": att8, "unit": UNIT, "cores": blas_threads(),
                                                 "kind": "oracle", "sample": desc8, "store_gbs": gbs8,
