@@ -8,9 +8,26 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <initializer_list>
 #include <utility>
 
 namespace h3kv {
+
+// True when both pointers are device memory aligned to 32 bytes: the store
+// builds then write codes with 32-byte stores (host-mapped buffers keep the
+// 16-byte stores).
+inline bool wide_store_ok(const void *a, const void *b) {
+  if (((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b)) & 31u) != 0) return false;
+  for (const void *p : {a, b}) {
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+      cudaGetLastError();  // clear the error the query may leave
+      return false;
+    }
+    if (attr.type != cudaMemoryTypeDevice) return false;
+  }
+  return true;
+}
 
 // Store build over `rows` = heads * seq rows of K and V.  Tensor maps: bf16
 // [rows, 128] inputs (box 64 x 128, 128B swizzle); int8 codes [rows, 128] and

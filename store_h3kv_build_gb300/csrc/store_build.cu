@@ -9,9 +9,9 @@
 // one producer warp streams bf16 tiles into a 3-stage shared-memory ring with
 // TMA (128-byte swizzle), and four compute warps own one row per thread (the
 // swizzle makes the per-row shared-memory reads bank-conflict free), run the
-// 128-point FWHT in registers, and store each row's codes (eight 16-byte
-// stores) and scale straight from registers.  The deeper ring and the direct
-// stores measured 6 % faster than a 2-stage ring with a staged TMA store.
+// 128-point FWHT in registers, and store each row's codes (four 32-byte
+// stores when the code buffers are 32-byte aligned, else eight 16-byte ones)
+// and scale straight from registers.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -58,8 +58,9 @@ __device__ __forceinline__ RowScale row_scale(float amax) {
 }
 
 // kGroups = 1: one scale per row; kGroups = 4: one per 32 consecutive
-// rotated values (the per-32-value variant).
-template <int kGroups>
+// rotated values (the per-32-value variant).  kWide: codes go out as 32-byte
+// stores (whole L2 sectors), for code buffers aligned to 32 bytes.
+template <int kGroups, bool kWide>
 __global__ void __launch_bounds__(kThreads, 2)
     store_build_kernel(const __grid_constant__ CUtensorMap tm_k_in, const __grid_constant__ CUtensorMap tm_v_in,
                        int8_t *__restrict__ k_codes, int8_t *__restrict__ v_codes,
@@ -176,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int64_t row0 = (is_v ? t - tiles_per_tensor : t) * kRows;
       const bool row_ok = row0 + r < rows;
       int8_t *oc = (is_v ? v_codes : k_codes) + (row_ok ? row0 + r : 0) * 128;
+      uint32_t wp[8];  // granules g - 1 and g, stored together when kWide
 #pragma unroll
       for (int g = 0; g < 8; ++g) {
         uint32_t w[4];
@@ -202,7 +204,13 @@ __global__ void __launch_bounds__(kThreads, 2)
           const uint32_t hi = __byte_perm(q[2], q[3], 0x0040);
           w[k] = __byte_perm(lo, hi, 0x5410);
         }
-        if (row_ok) *reinterpret_cast<uint4 *>(oc + g * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+        if constexpr (kWide) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) wp[(g & 1) * 4 + k] = w[k];
+          if ((g & 1) && row_ok) st_global_v8(oc + (g - 1) * 16, wp);
+        } else {
+          if (row_ok) *reinterpret_cast<uint4 *>(oc + g * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
       }
       uint16_t *scales = is_v ? v_scales : k_scales;
       if (row_ok) {
@@ -222,7 +230,11 @@ cudaError_t launch_store_build(const CUtensorMap &k_in, const CUtensorMap &v_in,
                                cudaStream_t stream) {
   const int64_t tiles = (rows + kRows - 1) / kRows;
   if (tiles == 0) return cudaSuccess;
-  auto kernel = scale_groups == 4 ? store_build_kernel<4> : store_build_kernel<1>;
+  // whole-sector stores: device code buffers aligned to 32 bytes (rows are
+  // multiples of 32 bytes, so every row's pairs of 16-byte pieces are too)
+  const bool wide = wide_store_ok(k_out, v_out);
+  auto kernel = scale_groups == 4 ? (wide ? store_build_kernel<4, true> : store_build_kernel<4, false>)
+                                  : (wide ? store_build_kernel<1, true> : store_build_kernel<1, false>);
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kBuildSmemBytes));
   if (e != cudaSuccess) return e;

@@ -8,8 +8,9 @@
 // GB300 design: the HBM-bound stream of the kvi8r build.  A persistent grid
 // (two CTAs per SM) walks 128-row tiles (K tiles, then V tiles); one producer
 // warp streams bf16 tiles into a 3-stage ring with TMA (128-byte swizzle), and
-// four compute warps own one row per thread and store its 64 code bytes and 8
-// scale bytes straight from registers.
+// four compute warps own one row per thread and store its 64 code bytes (two
+// 32-byte stores when the code buffers are 32-byte aligned, else four
+// 16-byte ones) and 8 scale bytes straight from registers.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -64,6 +65,7 @@ __device__ __forceinline__ uint2 encode_block(const float *x, float s, float r) 
   return w;
 }
 
+template <bool kWide>
 __global__ void __launch_bounds__(kThreads, 2)
     store_fp4_kernel(const __grid_constant__ CUtensorMap tm_k_in, const __grid_constant__ CUtensorMap tm_v_in,
                      uint8_t *__restrict__ k_codes, uint8_t *__restrict__ v_codes,
@@ -161,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       const bool row_ok = row0 + r < rows;
       uint8_t *oc = (is_v ? v_codes : k_codes) + (row_ok ? row0 + r : 0) * 64;
       uint32_t sw[2] = {0u, 0u};
+      uint32_t wp[8];  // chunks c - 1 and c, stored together when kWide
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         // blocks 2c and 2c + 1 fill 16-byte chunk c of the row's 64 code bytes
@@ -182,7 +185,15 @@ __global__ void __launch_bounds__(kThreads, 2)
           w[hb] = encode_block(xb, sf, sf > 0.f ? rcp_approx(sf) : 0.f);
           if (!(sf > 0.f)) w[hb] = make_uint2(0u, 0u);
         }
-        if (row_ok) *reinterpret_cast<uint4 *>(oc + c * 16) = make_uint4(w[0].x, w[0].y, w[1].x, w[1].y);
+        if constexpr (kWide) {
+          wp[(c & 1) * 4 + 0] = w[0].x;
+          wp[(c & 1) * 4 + 1] = w[0].y;
+          wp[(c & 1) * 4 + 2] = w[1].x;
+          wp[(c & 1) * 4 + 3] = w[1].y;
+          if ((c & 1) && row_ok) st_global_v8(oc + (c - 1) * 16, wp);
+        } else {
+          if (row_ok) *reinterpret_cast<uint4 *>(oc + c * 16) = make_uint4(w[0].x, w[0].y, w[1].x, w[1].y);
+        }
       }
       uint8_t *scales = is_v ? v_scales : k_scales;
       if (row_ok) *reinterpret_cast<uint2 *>(scales + (row0 + r) * 8) = make_uint2(sw[0], sw[1]);
@@ -198,12 +209,16 @@ cudaError_t launch_store_build_fp4(const CUtensorMap &k_in, const CUtensorMap &v
                                    int num_sms, uint32_t *err, uint64_t timeout_ns, cudaStream_t stream) {
   const int64_t tiles = (rows + kRows - 1) / kRows;
   if (tiles == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(store_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kFp4BuildSmemBytes));
+  // whole-sector stores: device code buffers aligned to 32 bytes (rows are
+  // multiples of 32 bytes, so every row's pairs of 16-byte pieces are too)
+  const bool wide = wide_store_ok(k_out, v_out);
+  auto kernel = wide ? store_fp4_kernel<true> : store_fp4_kernel<false>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kFp4BuildSmemBytes));
   if (e != cudaSuccess) return e;
   int64_t grid = static_cast<int64_t>(num_sms) * 2;
   if (grid > 2 * tiles) grid = 2 * tiles;
-  store_fp4_kernel<<<static_cast<unsigned>(grid), kThreads, kFp4BuildSmemBytes, stream>>>(
+  kernel<<<static_cast<unsigned>(grid), kThreads, kFp4BuildSmemBytes, stream>>>(
       k_in, v_in, k_out, v_out, k_scales, v_scales, rows, tiles, err, timeout_ns);
   return cudaGetLastError();
 }

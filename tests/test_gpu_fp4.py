@@ -324,3 +324,21 @@ def test_attend_fp4_every_kv_block(cuda):
         out = b.attend_fp4(q.to(cuda), st, q_chunk=128, kv_block=kvb)
         b.sync_status()
         compare_fp4_attention(out, q, g, f"kv_block={kvb}")
+
+
+def test_store_fp4_code_buffers_16_byte_aligned(cuda):
+    # 16- but not 32-byte aligned code buffers take the 16-byte store path
+    b = _b()
+    heads, seq = 2, 999
+    _, k, v = synth.make_qkv(heads, seq, seed=43, k_outliers=True, device=cuda)
+    ref = _build(k, v)
+    n = heads * seq * 64
+    kbuf = torch.empty(n + 32, dtype=torch.uint8, device=cuda)
+    vbuf = torch.empty(n + 32, dtype=torch.uint8, device=cuda)
+    kc, vc = kbuf[16:16 + n].view(heads, seq, 64), vbuf[16:16 + n].view(heads, seq, 64)
+    assert kc.data_ptr() % 32 == 16
+    odd = b.StoreFp4(kc, vc, torch.empty_like(ref.k_scales), torch.empty_like(ref.v_scales))
+    b.build_store_fp4(k, v, out=odd)
+    b.sync_status()
+    for name in ("k_codes", "v_codes", "k_scales", "v_scales"):
+        assert torch.equal(getattr(odd, name), getattr(ref, name)), name

@@ -108,3 +108,23 @@ def test_store_rotation_spreads_outliers(cuda):
     s_raw = oracle.row_scales(raw)
     raw_err = np.abs(oracle.dequant(oracle.quantize(raw, s_raw), s_raw) - raw)
     assert rot_err.mean() < 0.5 * raw_err.mean()
+
+
+@pytest.mark.parametrize("group", [0, 32])
+def test_store_build_code_buffers_16_byte_aligned(cuda, group):
+    # code buffers that are 16- but not 32-byte aligned take the 16-byte store
+    # path; the store must be the same bit for bit as in aligned buffers
+    from store_h3kv_build_gb300 import binding as b
+    heads, seq = 3, 1337
+    _, k, v = synth.make_qkv(heads, seq, seed=41, k_outliers=True, device=cuda)
+    ref = b.build_store(k, v, scale_group=group)
+    n = heads * seq * 128
+    kbuf = torch.empty(n + 32, dtype=torch.int8, device=cuda)
+    vbuf = torch.empty(n + 32, dtype=torch.int8, device=cuda)
+    kc, vc = kbuf[16:16 + n].view(heads, seq, 128), vbuf[16:16 + n].view(heads, seq, 128)
+    assert kc.data_ptr() % 32 == 16 and vc.data_ptr() % 32 == 16
+    odd = b.Store(kc, vc, torch.empty_like(ref.k_scales), torch.empty_like(ref.v_scales))
+    b.build_store(k, v, out=odd)
+    b.sync_status()
+    for name in ("k_codes", "v_codes", "k_scales", "v_scales"):
+        assert torch.equal(getattr(odd, name), getattr(ref, name)), name
