@@ -53,8 +53,7 @@ __device__ __forceinline__ float rcp_approx(float s) {
 }
 
 // Codes of one 16-value block x[0..15] with scale s > 0 (r ~ 1/s): e2m1 of
-// x / s.  Returns the 16 nibbles in two words, element 0
-// lowest.
+// x / s.  Returns the 16 nibbles in two words, element 0 lowest.
 __device__ __forceinline__ uint2 encode_block(const float *x, float s, float r) {
   float q[16];
 #pragma unroll
