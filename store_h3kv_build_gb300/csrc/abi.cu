@@ -494,9 +494,13 @@ h3kv_status h3kv_build_store_f8(const uint16_t *K, const uint16_t *V, int32_t he
   DeviceInfo *d = nullptr;
   h3kv_status st = device_info(&d);
   if (st != H3KV_OK) return st;
-  const cudaError_t e = h3kv::launch_store_build_f8(K, V, heads, seq, h3kv_f8_v_stride(seq), out->k_codes,
-                                                    out->v_codes_t, out->k_scales, out->v_scales, out->k_mean,
-                                                    d->err, g_timeout_ns.load(), static_cast<cudaStream_t>(stream));
+  CUtensorMap k_in, v_in;
+  if (!encode_3d_bf16(&k_in, K, static_cast<uint64_t>(seq), static_cast<uint64_t>(heads)) ||
+      !encode_3d_bf16(&v_in, V, static_cast<uint64_t>(seq), static_cast<uint64_t>(heads)))
+    return H3KV_ERR_CUDA;
+  const cudaError_t e = h3kv::launch_store_build_f8(
+      k_in, v_in, K, V, heads, seq, h3kv_f8_v_stride(seq), out->k_codes, out->v_codes_t, out->k_scales,
+      out->v_scales, out->k_mean, d->num_sms, d->err, g_timeout_ns.load(), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? H3KV_OK : H3KV_ERR_CUDA;
 }
 

@@ -90,11 +90,14 @@ cudaError_t launch_store_build_fp4(const CUtensorMap &k_in, const CUtensorMap &v
 cudaError_t launch_attend_fp4(const AttnArgs &args, bool overlap_previous, cudaStream_t stream);
 
 // kvf8s store build: statistics pass (K mean, V channel absmax) then the
-// encode pass.  V codes are written channel-major with row stride v_stride
-// (a multiple of 16, >= seq).
-cudaError_t launch_store_build_f8(const uint16_t *K, const uint16_t *V, int32_t heads, int64_t seq, int64_t v_stride,
-                                  uint8_t *k_codes, uint8_t *v_codes_t, float *k_scales, float *v_scales,
-                                  float *k_mean, uint32_t *err, uint64_t timeout_ns, cudaStream_t stream);
+// encode pass.  Tensor maps: bf16 [heads, seq, 128] inputs ({128, seq,
+// heads}, box 64 x 128 x 1, 128B swizzle; the statistics pass reads K and V
+// through the plain pointers).  V codes are written channel-major with row
+// stride v_stride (a multiple of 16, >= seq).
+cudaError_t launch_store_build_f8(const CUtensorMap &k_in, const CUtensorMap &v_in, const uint16_t *K,
+                                  const uint16_t *V, int32_t heads, int64_t seq, int64_t v_stride, uint8_t *k_codes,
+                                  uint8_t *v_codes_t, float *k_scales, float *v_scales, float *k_mean, int num_sms,
+                                  uint32_t *err, uint64_t timeout_ns, cudaStream_t stream);
 
 struct F8Args {
   const uint16_t *q;        // bf16 [heads, q_seq, 128]

@@ -26,7 +26,6 @@ namespace f8store {
 constexpr int kStatCtas = 16;     // one cluster of CTAs per head (8 where 16 cannot launch)
 constexpr int kStatThreads = 512;
 constexpr int kBlockTok = 64;     // tokens per K scale block
-constexpr int kEncThreads = 128;  // 4 warps x 16 tokens = one block
 constexpr float kE4m3Max = 448.0f;
 
 __device__ __forceinline__ void bf16x4(const uint2 w, float (&x)[4]) {
@@ -177,12 +176,6 @@ __global__ void __launch_bounds__(kStatThreads)
   cluster.sync();
 }
 
-// e4m3 codes of x * r for four values, r = fp32(1/s) (all zero when s == 0).
-__device__ __forceinline__ uint32_t encode4(const float (&x)[4], float s, float r) {
-  if (!(s > 0.f)) return 0u;
-  return pack_e4m3x4(__fmul_rn(x[0], r), __fmul_rn(x[1], r), __fmul_rn(x[2], r), __fmul_rn(x[3], r));
-}
-
 // Bytes c of words a, b, e, d (one per token) -> one word per channel c:
 // in-lane 4 x 4 byte transpose.
 __device__ __forceinline__ void transpose4x4(uint32_t a, uint32_t b, uint32_t e, uint32_t d, uint32_t (&out)[4]) {
@@ -194,128 +187,288 @@ __device__ __forceinline__ void transpose4x4(uint32_t a, uint32_t b, uint32_t e,
   out[3] = __byte_perm(t1, t3, 0x7632);
 }
 
+constexpr int kEncRows = 128;                  // tokens per tile = compute threads
+constexpr int kEncStages = 3;                  // input ring depth (2 CTAs per SM)
+constexpr int kEncTileBytes = kEncRows * 256;  // bf16 [128 tokens x 128 channels]
+constexpr int kEncThreads = kEncRows + 32;     // 4 compute warps + 1 producer warp
+
 struct EncSmem {
-  uint8_t k[kBlockTok * 256];  // the block's bf16 K rows
-  uint8_t v[kBlockTok * 256];  // and V rows
-  uint64_t full;
-  float warp_amax[kEncThreads / 32];
+  uint8_t in[kEncStages][kEncTileBytes];  // 1024-byte aligned (128-byte swizzle)
+  float neg_mu[128];   // -mean(k') of the current head
+  float rv[128];       // fp32(1 / s_v) per V channel, 0 where s_v = 0
+  uint32_t keep[32];   // byte mask of the V channels with s_v > 0
+  float warp_amax[4];  // K: per-warp absmax (warps 0-1: first 64 tokens of the tile)
+  uint64_t full[kEncStages];
+  uint64_t empty[kEncStages];
   int abort;
 };
+constexpr size_t kEncSmemBytes = sizeof(EncSmem) + 1024;
 
-// Pass 2, grid (blocks of 64 tokens, heads), 4 warps.  One bulk copy each
-// brings the block's K and V rows (contiguous within the head) into shared
-// memory; warp w then takes tokens 16w .. 16w+15, one token at a time across
-// the warp (lane l: channels 4l .. 4l+3).
-__global__ void __launch_bounds__(kEncThreads)
-    encode_kernel(const uint16_t *K, const uint16_t *V, int64_t seq, int64_t v_stride, const float *k_mean,
-                  const float *v_scales, uint8_t *k_codes, float *k_scales, uint8_t *v_codes_t, uint32_t *err,
-                  uint64_t timeout_ns) {
-  __shared__ __align__(128) EncSmem sm;
-  const int h = blockIdx.y;
-  const int64_t blk = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t blk0 = blk * kBlockTok;
-  const int64_t tok0 = blk0 + warp * 16;
-  const int64_t nblk = (seq + kBlockTok - 1) / kBlockTok;
-  const int64_t base = static_cast<int64_t>(h) * seq;
-  const int valid = static_cast<int>(seq - blk0 < kBlockTok ? seq - blk0 : kBlockTok);
-  const uint32_t bar = smem_u32(&sm.full);
+// Byte offset, inside a V tile's code staging area (the first 16 KB of the
+// drained input stage), of 16-byte granule g (channels 16g .. 16g+15) of
+// token row r.  The XOR pattern keeps the row writes (8 consecutive rows
+// per quarter-warp) and the column reads below (one 4-byte word of 32
+// rows r = 32 tq + k, k fixed per instruction) free of bank conflicts.
+__device__ __forceinline__ uint32_t vstage_off(uint32_t r, uint32_t g) {
+  return r * 128u + ((g ^ (r & 7u) ^ (2u * ((r >> 5) & 3u))) << 4);
+}
 
-  if (threadIdx.x == 0) {
-    mbar_init(bar, 1);
+// Pass 2, a persistent grid (two CTAs per SM) over tiles of 128 tokens of
+// one head, K and V tiles of the same tokens interleaved (tile u: token
+// chunk u / 2, V when u is odd); CTA b takes the contiguous tile range
+// [b n / grid, (b + 1) n / grid), so its head (and the per-head constants
+// held in shared memory) changes at most a few times.  One producer warp
+// fills a 3-stage ring with TMA (two 64-channel boxes per tile); the four
+// compute warps hold one token row per thread.
+//   K tile: the 128-point FWHT in registers (stage order stride 1 .. 64),
+//     k' = fp32(x / sqrt 128) - mu rounded to fp32, the absmax of each
+//     64-token block by a warp reduction and one 128-thread barrier, then
+//     the row's codes straight to global memory.
+//   V tile: the row's codes e4m3(v * fp32(1/s_v)) are written back into the
+//     drained stage, then each thread reads four channels of 32 tokens,
+//     transposes them in registers and stores 32-token pieces of four
+//     channel rows of the transposed V.
+// Tokens past seq arrive as zero rows (the 3-D map fills them): they give
+// zero V codes, which is what the transposed rows up to v_stride hold, and
+// are left out of the K absmax and stores.  kWide: 32-byte code stores.
+template <bool kWide>
+__global__ void __launch_bounds__(kEncThreads, 2)
+    encode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, int32_t heads,
+                  int64_t seq, int64_t v_stride, const float *__restrict__ k_mean,
+                  const float *__restrict__ v_scales, uint8_t *__restrict__ k_codes, float *__restrict__ k_scales,
+                  uint8_t *__restrict__ v_codes_t, uint32_t *err, uint64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  EncSmem &sm = *reinterpret_cast<EncSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t nch = (seq + kEncRows - 1) / kEncRows;    // token chunks per head
+  const int64_t nblk = (seq + kBlockTok - 1) / kBlockTok;  // K scale blocks per head
+  const int64_t n_tiles = 2 * static_cast<int64_t>(heads) * nch;
+  const int64_t u_begin = n_tiles * blockIdx.x / gridDim.x;
+  const int64_t u_end = n_tiles * (blockIdx.x + 1) / gridDim.x;
+
+  if (tid == 0) {
+    for (int st = 0; st < kEncStages; ++st) {
+      mbar_init(smem_u32(&sm.full[st]), 1);
+      mbar_init(smem_u32(&sm.empty[st]), kEncRows);
+    }
     sm.abort = 0;
     fence_mbar_init();
-    const uint32_t bytes = static_cast<uint32_t>(valid) * 256u;
-    mbar_arrive_expect_tx(bar, 2 * bytes);
-    bulk_g2s(smem_u32(sm.k), K + (base + blk0) * 128, bytes, bar);
-    bulk_g2s(smem_u32(sm.v), V + (base + blk0) * 128, bytes, bar);
-  }
-  // per-head constants load while the copies are in flight
-  float mu[4], rv[4];
-  uint32_t keep = 0u;  // byte mask of the V channels with a nonzero scale
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    mu[c] = k_mean[static_cast<int64_t>(h) * 128 + 4 * lane + c];
-    const float sv = v_scales[static_cast<int64_t>(h) * 128 + 4 * lane + c];
-    rv[c] = sv > 0.f ? __frcp_rn(sv) : 0.f;
-    keep |= (sv > 0.f ? 0xFFu : 0u) << (8 * c);
   }
   __syncthreads();
   const WaitCtx wctx{err, &sm.abort, timeout_ns};
-  if (!__syncthreads_and(mbar_wait(bar, 0, wctx))) {
-    // the copies must land before the CTA exits
-    if (threadIdx.x == 0) mbar_wait_drain(bar, 0, kDrainNs);
-    return;
-  }
 
-  // ---- K: rotate, smooth, block absmax, encode
-  float x[16][4];
-  float amax = 0.f;
+  if (warp == 4) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      int it = 0, issued = 0;
+      for (int64_t u = u_begin; u < u_end; ++u, ++it) {
+        const int st = it % kEncStages;
+        if (!mbar_wait(smem_u32(&sm.empty[st]), ((it / kEncStages) & 1) ^ 1, wctx)) break;
+        const int64_t idx = u >> 1;
+        const int32_t h = static_cast<int32_t>(idx / nch);
+        const int32_t tok0 = static_cast<int32_t>((idx - static_cast<int64_t>(h) * nch) * kEncRows);
+        const CUtensorMap *map = (u & 1) ? &tm_v : &tm_k;
+        const uint32_t bar = smem_u32(&sm.full[st]);
+        mbar_arrive_expect_tx(bar, kEncTileBytes);
+        tma_load_3d(smem_u32(sm.in[st]), map, 0, tok0, h, bar);
+        tma_load_3d(smem_u32(sm.in[st] + kEncTileBytes / 2), map, 64, tok0, h, bar);
+        ++issued;
+      }
+      if (sm.abort) {
+        // drain: every issued load must land before the CTA may exit
+        for (int k = (issued > kEncStages ? issued - kEncStages : 0); k < issued; ++k)
+          mbar_wait_drain(smem_u32(&sm.full[k % kEncStages]), (k / kEncStages) & 1, kDrainNs);
+      }
+    }
+  } else {
+    // ----------------------------------------------------------- compute
+    const uint32_t r = static_cast<uint32_t>(tid);  // token row within the tile
+    // transposed V read-back: channels 4 cg .. 4 cg + 3 of tokens 32 tq .. 32 tq + 31
+    const uint32_t cg = r >> 2, tq = r & 3;
+    const uint32_t rd_base = tq * 32u * 128u + (cg & 3u) * 4u;
+    const uint32_t rd_gx = (cg >> 2) ^ (2u * tq);
+    int64_t cur_h = -1;
+    int it = 0;
+    for (int64_t u = u_begin; u < u_end; ++u, ++it) {
+      const int st = it % kEncStages;
+      const bool is_v = (u & 1) != 0;
+      const int64_t idx = u >> 1;
+      const int64_t h = idx / nch;
+      const int64_t c = idx - h * nch;
+      const int64_t tok0 = c * kEncRows;
+      const int valid = static_cast<int>(seq - tok0 < kEncRows ? seq - tok0 : kEncRows);
+      if (h != cur_h) {
+        // the head's constants, once every thread is done with the last head's
+        const float mu = k_mean[h * 128 + r];
+        const float sv = v_scales[h * 128 + r];
+        named_bar_sync(1, kEncRows);
+        sm.neg_mu[r] = -mu;
+        sm.rv[r] = sv > 0.f ? __frcp_rn(sv) : 0.f;
+        reinterpret_cast<uint8_t *>(sm.keep)[r] = sv > 0.f ? 0xFFu : 0u;
+        named_bar_sync(1, kEncRows);
+        cur_h = h;
+      }
+      // every compute thread takes the same decision (a wait that gave up on
+      // one thread stops all of them together)
+      const bool ok = mbar_wait(smem_u32(&sm.full[st]), (it / kEncStages) & 1, wctx);
+      if (!named_bar_and(1, kEncRows, ok)) break;
+      uint8_t *tile = sm.in[st];
+
+      if (!is_v) {
+        float x[128];
 #pragma unroll
-  for (int t = 0; t < 16; ++t) {
-    const int lr = warp * 16 + t;
-    if (lr < valid) {
-      bf16x4(*reinterpret_cast<const uint2 *>(sm.k + lr * 256 + 8 * lane), x[t]);
-      fwht128_warp(x[t], lane);
+        for (int hc = 0; hc < 2; ++hc) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        // k' rounded to fp32 before the mean is taken off (no fused rounding)
-        x[t][c] = __fsub_rn(__fmul_rn(x[t][c], kInvSqrt128), mu[c]);
-        amax = fmaxf(amax, fabsf(x[t][c]));
+          for (int g = 0; g < 8; ++g) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(tile + hc * (kEncTileBytes / 2) + sw128_off(r, g));
+            const int e = hc * 64 + g * 8;
+            x[e + 0] = bf16lo_to_f32(w.x);
+            x[e + 1] = bf16hi_to_f32(w.x);
+            x[e + 2] = bf16lo_to_f32(w.y);
+            x[e + 3] = bf16hi_to_f32(w.y);
+            x[e + 4] = bf16lo_to_f32(w.z);
+            x[e + 5] = bf16hi_to_f32(w.z);
+            x[e + 6] = bf16lo_to_f32(w.w);
+            x[e + 7] = bf16hi_to_f32(w.w);
+          }
+        }
+        mbar_arrive(smem_u32(&sm.empty[st]));
+        fwht128_packed(x);  // x = sqrt(128) * (row H)
+        // k' = x / sqrt(128) rounded to fp32, then the mean taken off: two
+        // scalar roundings (__fmul_rn / __fadd_rn are never contracted into
+        // an fma; a packed multiply followed by a packed add was, which left
+        // the product's rounding error in k' - mu)
+        float am[2] = {0.f, 0.f};
+#pragma unroll
+        for (int e = 0; e < 128; e += 4) {
+          const float4 nm = *reinterpret_cast<const float4 *>(&sm.neg_mu[e]);
+          x[e] = __fadd_rn(__fmul_rn(x[e], kInvSqrt128), nm.x);
+          x[e + 1] = __fadd_rn(__fmul_rn(x[e + 1], kInvSqrt128), nm.y);
+          x[e + 2] = __fadd_rn(__fmul_rn(x[e + 2], kInvSqrt128), nm.z);
+          x[e + 3] = __fadd_rn(__fmul_rn(x[e + 3], kInvSqrt128), nm.w);
+          am[0] = fmax3(am[0], fabsf(x[e]), fabsf(x[e + 1]));
+          am[1] = fmax3(am[1], fabsf(x[e + 2]), fabsf(x[e + 3]));
+        }
+        float amax = static_cast<int>(r) < valid ? fmaxf(am[0], am[1]) : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (lane == 0) sm.warp_amax[warp] = amax;
+        named_bar_sync(1, kEncRows);
+        // block of 64 tokens: warps 0-1 or 2-3 (a warp never straddles two)
+        const float bmax = fmaxf(sm.warp_amax[warp & ~1], sm.warp_amax[warp | 1]);
+        const float s = __fdiv_rn(bmax, kE4m3Max);
+        const float rs = s > 0.f ? __frcp_rn(s) : 0.f;
+        if (static_cast<int>(r) < valid) {
+          if ((r & 63u) == 0u) k_scales[h * nblk + 2 * c + (r >> 6)] = s;
+          uint8_t *dst = k_codes + (h * seq + tok0 + r) * 128;
+          const float2 rs2 = make_float2(rs, rs);
+          uint32_t wp[8];  // granules g - 1 and g, stored together when kWide
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int e = g * 16 + k * 4;
+              const float2 a = __fmul2_rn(make_float2(x[e], x[e + 1]), rs2);
+              const float2 b = __fmul2_rn(make_float2(x[e + 2], x[e + 3]), rs2);
+              // a block whose scale is 0 (or not a number) gets zero codes
+              w[k] = s > 0.f ? pack_e4m3x4(a.x, a.y, b.x, b.y) : 0u;
+            }
+            if constexpr (kWide) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) wp[(g & 1) * 4 + k] = w[k];
+              if (g & 1) st_global_v8(dst + (g - 1) * 16, wp);
+            } else {
+              *reinterpret_cast<uint4 *>(dst + g * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      } else {
+        // codes of the row, 16 channels (one input granule pair) at a time
+        uint32_t w[32];
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int gi = 2 * g + hf;  // input granule: channels 8 gi .. 8 gi + 7
+            const uint4 in =
+                *reinterpret_cast<const uint4 *>(tile + (gi >> 3) * (kEncTileBytes / 2) + sw128_off(r, gi & 7));
+            const float4 r0 = *reinterpret_cast<const float4 *>(&sm.rv[8 * gi]);
+            const float4 r1 = *reinterpret_cast<const float4 *>(&sm.rv[8 * gi + 4]);
+            float v[8];
+            bf16x4(make_uint2(in.x, in.y), *reinterpret_cast<float(*)[4]>(v));
+            bf16x4(make_uint2(in.z, in.w), *reinterpret_cast<float(*)[4]>(v + 4));
+            w[2 * gi] = pack_e4m3x4(__fmul_rn(v[0], r0.x), __fmul_rn(v[1], r0.y), __fmul_rn(v[2], r0.z),
+                                    __fmul_rn(v[3], r0.w));
+            w[2 * gi + 1] = pack_e4m3x4(__fmul_rn(v[4], r1.x), __fmul_rn(v[5], r1.y), __fmul_rn(v[6], r1.z),
+                                        __fmul_rn(v[7], r1.w));
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const uint4 kp = *reinterpret_cast<const uint4 *>(&sm.keep[4 * g]);
+          w[4 * g] &= kp.x;
+          w[4 * g + 1] &= kp.y;
+          w[4 * g + 2] &= kp.z;
+          w[4 * g + 3] &= kp.w;
+        }
+        named_bar_sync(1, kEncRows);  // every row of the stage has been read
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          *reinterpret_cast<uint4 *>(tile + vstage_off(r, g)) =
+              make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+        named_bar_sync(1, kEncRows);  // the staged codes are complete
+        uint32_t col[4][8];  // [channel][group of 4 tokens]
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint32_t t4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t k = 4u * j + i;  // token 32 tq + k; (32 tq + k) & 7 = k & 7
+            t4[i] = *reinterpret_cast<const uint32_t *>(tile + rd_base + k * 128u + ((rd_gx ^ (k & 7u)) << 4));
+          }
+          uint32_t o[4];
+          transpose4x4(t4[0], t4[1], t4[2], t4[3], o);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) col[cc][j] = o[cc];
+        }
+        // the stage goes back to the TMA (async proxy) after these generic writes
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&sm.empty[st]));
+        // tokens tok0 + 32 tq .. + 31; v_stride is a multiple of 16, so a
+        // piece is whole, half (the last 16 tokens of the padded row) or past it
+        const int64_t t_first = tok0 + 32 * static_cast<int64_t>(tq);
+        const int64_t rem = v_stride - t_first;
+        if (rem > 0) {
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            uint8_t *dst = v_codes_t + (h * 128 + 4 * cg + cc) * v_stride + t_first;
+            if (rem >= 32) {
+              if constexpr (kWide) {
+                st_global_v8(dst, col[cc]);
+              } else {
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(col[cc][0], col[cc][1], col[cc][2], col[cc][3]);
+                *reinterpret_cast<uint4 *>(dst + 16) = make_uint4(col[cc][4], col[cc][5], col[cc][6], col[cc][7]);
+              }
+            } else {
+              *reinterpret_cast<uint4 *>(dst) = make_uint4(col[cc][0], col[cc][1], col[cc][2], col[cc][3]);
+            }
+          }
+        }
       }
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  if (lane == 0) sm.warp_amax[warp] = amax;
   __syncthreads();
-  const float bmax = fmaxf(fmaxf(sm.warp_amax[0], sm.warp_amax[1]), fmaxf(sm.warp_amax[2], sm.warp_amax[3]));
-  const float s = __fdiv_rn(bmax, kE4m3Max);
-  const float rs = s > 0.f ? __frcp_rn(s) : 0.f;
-  if (threadIdx.x == 0) k_scales[static_cast<int64_t>(h) * nblk + blk] = s;
-#pragma unroll
-  for (int t = 0; t < 16; ++t) {
-    const int64_t tok = tok0 + t;
-    if (tok < seq) *reinterpret_cast<uint32_t *>(k_codes + (base + tok) * 128 + 4 * lane) = encode4(x[t], s, rs);
-  }
-
-  // ---- V: per-channel scales, encode, write transposed
-  uint32_t w[16];
-#pragma unroll
-  for (int t = 0; t < 16; ++t) {
-    const int lr = warp * 16 + t;
-    w[t] = 0u;
-    if (lr < valid) {
-      float v[4];
-      bf16x4(*reinterpret_cast<const uint2 *>(sm.v + lr * 256 + 8 * lane), v);
-      w[t] = pack_e4m3x4(__fmul_rn(v[0], rv[0]), __fmul_rn(v[1], rv[1]), __fmul_rn(v[2], rv[2]),
-                         __fmul_rn(v[3], rv[3])) & keep;
-    }
-  }
-  // 16 tokens x 4 channels -> 4 channel rows of 16 bytes; padding tokens
-  // (past seq, inside v_stride) are written as zero codes
-  if (tok0 < v_stride) {
-    uint32_t col[4][4];  // [channel][token group of 4]
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      uint32_t o[4];
-      transpose4x4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3], o);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) col[c][g] = o[c];
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint8_t *dst = v_codes_t + (static_cast<int64_t>(h) * 128 + 4 * lane + c) * v_stride + tok0;
-      *reinterpret_cast<uint4 *>(dst) = make_uint4(col[c][0], col[c][1], col[c][2], col[c][3]);
-    }
-  }
 }
 
 }  // namespace f8store
 
-cudaError_t launch_store_build_f8(const uint16_t *K, const uint16_t *V, int32_t heads, int64_t seq, int64_t v_stride,
-                                  uint8_t *k_codes, uint8_t *v_codes_t, float *k_scales, float *v_scales,
-                                  float *k_mean, uint32_t *err, uint64_t timeout_ns, cudaStream_t stream) {
+cudaError_t launch_store_build_f8(const CUtensorMap &k_in, const CUtensorMap &v_in, const uint16_t *K,
+                                  const uint16_t *V, int32_t heads, int64_t seq, int64_t v_stride, uint8_t *k_codes,
+                                  uint8_t *v_codes_t, float *k_scales, float *v_scales, float *k_mean, int num_sms,
+                                  uint32_t *err, uint64_t timeout_ns, cudaStream_t stream) {
   if (heads <= 0 || seq <= 0) return cudaSuccess;
   // statistics: one 16-CTA cluster per head (a non-portable size), else 8
   cudaError_t e = cudaFuncSetAttribute(f8store::stats_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -348,10 +501,18 @@ cudaError_t launch_store_build_f8(const uint16_t *K, const uint16_t *V, int32_t 
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t nblk = (seq + f8store::kBlockTok - 1) / f8store::kBlockTok;
-  f8store::encode_kernel<<<dim3(static_cast<unsigned>(nblk), static_cast<unsigned>(heads)), f8store::kEncThreads, 0,
-                           stream>>>(K, V, seq, v_stride, k_mean, v_scales, k_codes, k_scales, v_codes_t, err,
-                                     timeout_ns);
+  // whole-sector stores: device code buffers aligned to 32 bytes and V rows
+  // of a multiple of 32 bytes
+  const bool wide = wide_store_ok(k_codes, v_codes_t) && v_stride % 32 == 0;
+  auto kernel = wide ? f8store::encode_kernel<true> : f8store::encode_kernel<false>;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(f8store::kEncSmemBytes));
+  if (e != cudaSuccess) return e;
+  const int64_t n_tiles = 2 * static_cast<int64_t>(heads) * ((seq + f8store::kEncRows - 1) / f8store::kEncRows);
+  int64_t grid = 2 * static_cast<int64_t>(num_sms);
+  if (grid > n_tiles) grid = n_tiles;
+  kernel<<<static_cast<unsigned>(grid), f8store::kEncThreads, f8store::kEncSmemBytes, stream>>>(
+      k_in, v_in, heads, seq, v_stride, k_mean, v_scales, k_codes, k_scales, v_codes_t, err, timeout_ns);
   return cudaGetLastError();
 }
 

@@ -168,6 +168,39 @@ def test_store_f8_deterministic(cuda):
         assert torch.equal(getattr(a, name), getattr(b2, name)), name
 
 
+def test_store_f8_single_token_heads_smooth_to_zero(cuda):
+    # one token per head: the head's mean is the token itself, so k' - mu is
+    # exactly zero when k' and mu are each rounded to fp32 before the
+    # subtraction (a fused multiply-add would leave the product's rounding
+    # error there): every K scale and K code is zero
+    b = _b()
+    _, k, v = synth.make_qkv(6, 1, seed=33, k_outliers=True, device=cuda)
+    st = _build(k, v)
+    assert not st.k_scales.any() and not st.k_codes.any()
+    assert bool((st.v_scales > 0).all())
+
+
+def test_store_f8_code_buffers_16_byte_aligned(cuda):
+    # code buffers that are 16- but not 32-byte aligned take the 16-byte store
+    # path of the encode pass; the store must be the same bit for bit
+    b = _b()
+    heads, seq = 3, 1344  # V rows of 1344 bytes: a multiple of 32
+    _, k, v = synth.make_qkv(heads, seq, seed=42, k_outliers=True, device=cuda)
+    ref = _build(k, v)
+    nk, nv = heads * seq * 128, ref.v_codes_t.numel()
+    kbuf = torch.empty(nk + 32, dtype=torch.uint8, device=cuda)
+    vbuf = torch.empty(nv + 32, dtype=torch.uint8, device=cuda)
+    kc = kbuf[16:16 + nk].view(heads, seq, 128)
+    vc = vbuf[16:16 + nv].view(ref.v_codes_t.shape)
+    assert kc.data_ptr() % 32 == 16 and vc.data_ptr() % 32 == 16
+    odd = b.StoreF8(kc, vc, torch.empty_like(ref.k_scales), torch.empty_like(ref.v_scales),
+                    torch.empty_like(ref.k_mean), seq)
+    b.build_store_f8(k, v, out=odd)
+    b.sync_status()
+    for name in ("k_codes", "v_codes_t", "k_scales", "v_scales", "k_mean"):
+        assert torch.equal(getattr(odd, name), getattr(ref, name)), name
+
+
 def test_store_f8_h24_l32768_outlier(cuda):
     w = synth.WORKLOADS["h24_l32768_outlier"]
     q, k, v = synth.make_qkv(w["heads"], w["seq"], seed=0, k_outliers=True)
