@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define H3KV_ABI_VERSION 4u
+#define H3KV_ABI_VERSION 5u
 #define H3KV_HEAD_DIM 128
 /* kv_block = 0 on the kvi8r path means this many tokens (the kv_block
  * default of the kv_store row). */
@@ -155,8 +155,9 @@ h3kv_status h3kv_attend_staged(const uint16_t *Q, int64_t q_seq, const h3kv_stor
                                size_t staging_bytes, float *state, void *stream);
 
 /* Device scratch bytes h3kv_attend_hostio needs: two query chunks of Q
- * (bf16) and two of O (fp32) for every head, 2 * heads * q_chunk * 128 * 6.
- * Returns 0 for invalid arguments. */
+ * (bf16) and two of O (fp32) for every head, plus 256 bytes for the two
+ * buffers' ready words: 2 * heads * q_chunk * 128 * 6 + 256.  Returns 0 for
+ * invalid arguments. */
 size_t h3kv_hostio_scratch_bytes(int32_t heads, int32_t q_chunk);
 
 /* h3kv_attend with Q and O in host memory (pinned for asynchronous copies),
@@ -164,8 +165,14 @@ size_t h3kv_hostio_scratch_bytes(int32_t heads, int32_t q_chunk);
  * of bounding the device transient.  The rows of chunk c are copied in, attended over
  * the (device-resident) store, and copied back.  The copies of other chunks
  * run on a second stream that the library creates for the call, so they
- * overlap the attention of chunk c.  The result is bit-identical to
- * h3kv_attend with device Q and O and the same q_chunk and kv_block.
+ * overlap the attention of chunk c.  The chunk launches follow each other
+ * as in h3kv_attend (each may start on the SMs the previous one's tail
+ * frees): a launch waits inside the kernel, bounded by the wait limit, for
+ * a ready word in the scratch that the copy stream sets once the chunk's Q
+ * rows are in and its O buffer is free.  The 4-byte values come from a 4 KB
+ * pinned host table that the library allocates on the first call and keeps
+ * until the process exits.  The result is bit-identical to h3kv_attend with
+ * device Q and O and the same q_chunk and kv_block.
  *   Q_host: bf16 [store->heads, q_seq, 128]; O_host: fp32, same shape.
  *   scratch: device memory >= h3kv_hostio_scratch_bytes(store->heads,
  *   q_chunk), 16-byte aligned, caller-owned, reused by each call (calls that

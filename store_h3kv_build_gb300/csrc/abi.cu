@@ -129,6 +129,10 @@ constexpr int64_t kMaxRows = (1ll << 31) - 256;
 // The attention kernels run one grid row per head (grid.y <= 65535).
 constexpr int32_t kMaxHeads = 65535;
 
+// hostio scratch: the two chunk buffers' ready words, padded to keep the
+// region a multiple of 256 bytes.
+constexpr size_t kHostioReadyBytes = 256;
+
 h3kv_status check_chunks(int32_t q_chunk, int32_t kv_block) {
   if (q_chunk < 1) return H3KV_ERR_INVALID_ARG;
   if (kv_block < 0 || kv_block % H3KV_KV_TILE != 0) return H3KV_ERR_INVALID_ARG;
@@ -366,8 +370,32 @@ h3kv_status h3kv_attend_staged(const uint16_t *Q, int64_t q_seq, const h3kv_stor
 
 size_t h3kv_hostio_scratch_bytes(int32_t heads, int32_t q_chunk) {
   if (heads < 0 || q_chunk < 1) return 0;
-  return 2 * static_cast<size_t>(heads) * static_cast<size_t>(q_chunk) * H3KV_HEAD_DIM * (2 + 4);
+  return 2 * static_cast<size_t>(heads) * static_cast<size_t>(q_chunk) * H3KV_HEAD_DIM * (2 + 4) + kHostioReadyBytes;
 }
+
+namespace {
+
+// Values the copy engine writes into hostio's ready words: entries 0 and 1
+// are zero (the reset), entry v holds v.  Pinned host memory, so that the
+// 4-byte copies run on the copy engine; allocated once, kept until exit.
+constexpr int kReadyValues = 1024;
+std::mutex g_ready_mu;
+uint32_t *g_ready_table = nullptr;
+
+const uint32_t *ready_table() {
+  std::lock_guard<std::mutex> lock(g_ready_mu);
+  if (!g_ready_table) {
+    void *p = nullptr;
+    if (cudaHostAlloc(&p, kReadyValues * sizeof(uint32_t), cudaHostAllocPortable) != cudaSuccess) return nullptr;
+    uint32_t *t = static_cast<uint32_t *>(p);
+    t[0] = t[1] = 0;
+    for (int v = 2; v < kReadyValues; ++v) t[v] = static_cast<uint32_t>(v);
+    g_ready_table = t;
+  }
+  return g_ready_table;
+}
+
+}  // namespace
 
 h3kv_status h3kv_attend_hostio(const uint16_t *Q_host, int64_t q_seq, const h3kv_store *store, int32_t q_chunk,
                                int32_t kv_block, float softmax_scale, float *O_host, void *scratch,
@@ -392,8 +420,11 @@ h3kv_status h3kv_attend_hostio(const uint16_t *Q_host, int64_t q_seq, const h3kv
   DeviceInfo *d = nullptr;
   st = device_info(&d);
   if (st != H3KV_OK) return st;
+  const uint32_t *table = ready_table();
+  if (!table) return H3KV_ERR_CUDA;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // scratch: Q chunks [2][H, q_chunk, 128] bf16, then O chunks [2][H, q_chunk, 128] fp32
+  // scratch: Q chunks [2][H, q_chunk, 128] bf16, O chunks [2][H, q_chunk, 128]
+  // fp32, then the two buffers' ready words
   const int64_t qc = q_chunk;
   uint16_t *qbuf[2];
   float *obuf[2];
@@ -401,6 +432,7 @@ h3kv_status h3kv_attend_hostio(const uint16_t *Q_host, int64_t q_seq, const h3kv
   qbuf[1] = qbuf[0] + H * qc * 128;
   obuf[0] = reinterpret_cast<float *>(qbuf[1] + H * qc * 128);
   obuf[1] = obuf[0] + H * qc * 128;
+  uint32_t *ready = reinterpret_cast<uint32_t *>(obuf[1] + H * qc * 128);
   const int32_t kvb = kv_block == 0 ? H3KV_DEFAULT_KV_BLOCK : kv_block;
   h3kv::AttnArgs a{};
   a.k_codes = store->k_codes;
@@ -418,10 +450,20 @@ h3kv_status h3kv_attend_hostio(const uint16_t *Q_host, int64_t q_seq, const h3kv
   a.timeout_ns = g_timeout_ns.load();
   a.q_begin = 0;
 
-  // the copy stream and the events live for this call only (destroying them
-  // with work pending is allowed: they are released once it completes)
+  // Schedule.  Copy stream cs: reset both ready words, Q chunks 0 and 1 in;
+  // then, per chunk c, once its attention is done: O chunk c out, Q chunk
+  // c + 2 into the freed buffer, and that buffer's ready word set to the
+  // value of chunk c + 2.  Caller's stream s: chunk 0's launch waits for its
+  // Q copy (an event); launches 1 .. n-1 follow each other with programmatic
+  // dependent launch and wait for their ready word inside the kernel, so no
+  // stream wait sits between them (one would end the overlap of a launch's
+  // tail with the next launch).  Progress: the word of chunk c needs chunk
+  // c - 2 complete, and every CTA of chunk c - 2 is running or done before
+  // chunk c can launch (c - 1 launches only after all of c - 2's CTAs have
+  // started, c only after all of c - 1's), so a waiting CTA always sees its
+  // word arrive.
   cudaStream_t cs = nullptr;
-  cudaEvent_t entry = nullptr, fin = nullptr, q_ready[2] = {nullptr, nullptr}, att_done[2] = {nullptr, nullptr};
+  cudaEvent_t entry = nullptr, fin = nullptr, q0_ready = nullptr, att_done[2] = {nullptr, nullptr};
   h3kv_status result = H3KV_OK;
   auto fail = [&](cudaError_t e) {
     if (e != cudaSuccess && result == H3KV_OK) result = H3KV_ERR_CUDA;
@@ -429,11 +471,13 @@ h3kv_status h3kv_attend_hostio(const uint16_t *Q_host, int64_t q_seq, const h3kv
   };
   const unsigned ef = cudaEventDisableTiming;
   if (!fail(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking)) && !fail(cudaEventCreateWithFlags(&entry, ef)) &&
-      !fail(cudaEventCreateWithFlags(&fin, ef)) && !fail(cudaEventCreateWithFlags(&q_ready[0], ef)) &&
-      !fail(cudaEventCreateWithFlags(&q_ready[1], ef)) && !fail(cudaEventCreateWithFlags(&att_done[0], ef)) &&
-      !fail(cudaEventCreateWithFlags(&att_done[1], ef))) {
+      !fail(cudaEventCreateWithFlags(&fin, ef)) && !fail(cudaEventCreateWithFlags(&q0_ready, ef)) &&
+      !fail(cudaEventCreateWithFlags(&att_done[0], ef)) && !fail(cudaEventCreateWithFlags(&att_done[1], ef))) {
     const int64_t n = (q_seq + qc - 1) / qc;
     auto rows_of = [&](int64_t c) { return (c + 1) * qc <= q_seq ? qc : q_seq - c * qc; };
+    // ready value of chunk c >= 1: never 0 (the reset) and different from
+    // chunk c - 2's, the previous value of the same word
+    auto value_of = [](int64_t c) { return static_cast<uint32_t>(2 + c % (kReadyValues - 2)); };
     // Q rows [c qc, c qc + rows) of every head -> chunk buffer b
     auto copy_in = [&](int64_t c, int b) {
       return cudaMemcpy2DAsync(qbuf[b], qc * 256, Q_host + c * qc * 128, q_seq * 256, rows_of(c) * 256, H,
@@ -443,26 +487,32 @@ h3kv_status h3kv_attend_hostio(const uint16_t *Q_host, int64_t q_seq, const h3kv
       return cudaMemcpy2DAsync(O_host + c * qc * 128, q_seq * 512, obuf[b], qc * 512, rows_of(c) * 512, H,
                                cudaMemcpyDeviceToHost, cs);
     };
+    auto set_ready = [&](int64_t c) {
+      return cudaMemcpyAsync(&ready[c & 1], &table[value_of(c)], sizeof(uint32_t), cudaMemcpyHostToDevice, cs);
+    };
     // the copies start after everything queued on the caller's stream
-    bool ok = !fail(cudaEventRecord(entry, s)) && !fail(cudaStreamWaitEvent(cs, entry, 0));
-    for (int64_t c = 0; ok && c < 2 && c < n; ++c)
-      ok = !fail(copy_in(c, static_cast<int>(c))) && !fail(cudaEventRecord(q_ready[c], cs));
+    bool ok = !fail(cudaEventRecord(entry, s)) && !fail(cudaStreamWaitEvent(cs, entry, 0)) &&
+              !fail(cudaMemcpyAsync(ready, table, 2 * sizeof(uint32_t), cudaMemcpyHostToDevice, cs)) &&
+              !fail(copy_in(0, 0)) && !fail(cudaEventRecord(q0_ready, cs));
+    if (ok && n > 1) ok = !fail(copy_in(1, 1)) && !fail(set_ready(1));
     for (int64_t c = 0; ok && c < n; ++c) {
       const int b = static_cast<int>(c & 1);
       a.q = qbuf[b];
       a.o = obuf[b];
       a.q_end = rows_of(c);
-      ok = !fail(cudaStreamWaitEvent(s, q_ready[b], 0)) && !fail(h3kv::launch_attend_kvi8r(a, false, s)) &&
-           !fail(cudaEventRecord(att_done[b], s)) && !fail(cudaStreamWaitEvent(cs, att_done[b], 0)) &&
-           !fail(copy_out(c, b));
+      a.q_ready = c > 0 ? &ready[b] : nullptr;
+      a.q_ready_value = c > 0 ? value_of(c) : 0u;
+      if (c == 0) ok = !fail(cudaStreamWaitEvent(s, q0_ready, 0));
+      ok = ok && !fail(h3kv::launch_attend_kvi8r(a, c > 0, s)) && !fail(cudaEventRecord(att_done[b], s)) &&
+           !fail(cudaStreamWaitEvent(cs, att_done[b], 0)) && !fail(copy_out(c, b));
       // buffer b is free again for chunk c + 2 once its O rows are out
-      if (ok && c + 2 < n) ok = !fail(copy_in(c + 2, b)) && !fail(cudaEventRecord(q_ready[b], cs));
+      if (ok && c + 2 < n) ok = !fail(copy_in(c + 2, b)) && !fail(set_ready(c + 2));
     }
     // later work on the caller's stream sees every O row in host memory
     if (ok) ok = !fail(cudaEventRecord(fin, cs)) && !fail(cudaStreamWaitEvent(s, fin, 0));
     (void)ok;
   }
-  for (cudaEvent_t e : {entry, fin, q_ready[0], q_ready[1], att_done[0], att_done[1]})
+  for (cudaEvent_t e : {entry, fin, q0_ready, att_done[0], att_done[1]})
     if (e) cudaEventDestroy(e);
   if (cs) cudaStreamDestroy(cs);
   return result;

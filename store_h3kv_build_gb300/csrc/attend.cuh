@@ -270,6 +270,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = static_cast<int>((a.kv_seq + kBN - 1) / kBN);
   const int blk = a.kv_block_tiles;
 
+  if (a.q_ready != nullptr) {
+    // a query chunk streamed from host memory: its Q rows and O buffer are
+    // ready once the copy engine has written the launch's value (before any
+    // TMEM is taken, so a waiting CTA holds nothing the previous launch needs)
+    if (tid == 0) sm.abort = wait_word_equal(a.q_ready, a.q_ready_value, a.err, a.timeout_ns) ? 0 : 1;
+    __syncthreads();
+    if (sm.abort) {
+      if (tid == 0) pdl_wait_prerequisites();
+      return;
+    }
+  }
+
   if (tid == 0) {
     mbar_init(smem_u32(&sm.q_full), kKvi8r ? kNQ * kBM : 1);
     for (int s = 0; s < kNK; ++s) {
@@ -325,8 +337,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int rr = 0; rr < 32; ++rr) {
         const int64_t r = row0 + q * kBM + wq * 32 + rr;
-        buf[rr] = r < a.q_end ? *reinterpret_cast<const uint2 *>(a.q + (static_cast<int64_t>(h) * a.q_seq + r) * 128 +
-                                                                  4 * lane)
+        // through L2 (ld.global.cg): a streamed chunk's buffer is rewritten
+        // by the copy engine between launches that may share an SM
+        buf[rr] = r < a.q_end ? __ldcg(reinterpret_cast<const uint2 *>(a.q + (static_cast<int64_t>(h) * a.q_seq + r) *
+                                                                                   128 +
+                                                                       4 * lane))
                               : make_uint2(0u, 0u);
       }
 #pragma unroll

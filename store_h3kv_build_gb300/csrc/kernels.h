@@ -63,6 +63,12 @@ struct AttnArgs {
   float2 *state;
   int32_t stage_flags;
   int32_t scale_groups;     // kvi8r scales per row: 1, or 4 (one per 32 values)
+  // Query chunks streamed from host memory: when q_ready is set, every CTA
+  // first waits (bounded) until the word equals q_ready_value, which the copy
+  // engine writes once this launch's Q rows are in place and its O buffer is
+  // free; nullptr: no wait.
+  const uint32_t *q_ready;
+  uint32_t q_ready_value;
 };
 
 constexpr int kAttnRowsPerCta = 256;  // two 128-row query tiles per CTA

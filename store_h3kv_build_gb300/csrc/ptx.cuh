@@ -92,6 +92,28 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   return true;
 }
 
+// Bounded wait until a global word, written by a copy engine, equals `v`.
+// Polls with an acquire load (the copy's data lands before the word, and the
+// loads after the wait go to L2) and backs off with nanosleep between polls.
+// Returns false after recording the timeout if the limit runs out.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool wait_word_equal(const uint32_t *p, uint32_t v, uint32_t *err, uint64_t timeout_ns) {
+  if (ld_acquire_gpu(p) == v) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire_gpu(p) != v) {
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+    __nanosleep(256);
+  }
+  return true;
+}
+
 // Bounded wait used while draining after an abort: ignores the abort flag.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
   if (mbar_try_wait(bar, parity)) return true;

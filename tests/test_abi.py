@@ -31,7 +31,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_abi_version_and_strings():
-    assert b.h3kv_abi_version() == 4
+    assert b.h3kv_abi_version() == 5
     for st in range(5):
         assert b.h3kv_strerror(st)
     assert b.h3kv_strerror(99) == b"unknown status"
@@ -170,7 +170,7 @@ def test_attend_f8_rejects_bad_arguments():
 
 
 def test_hostio_checks():
-    assert b.h3kv_hostio_scratch_bytes(32, 16384) == 2 * 32 * 16384 * 128 * 6
+    assert b.h3kv_hostio_scratch_bytes(32, 16384) == 2 * 32 * 16384 * 128 * 6 + 256
     assert b.h3kv_hostio_scratch_bytes(1, 0) == 0 and b.h3kv_hostio_scratch_bytes(-1, 10) == 0
     st = _store()
     hi = b.h3kv_attend_hostio

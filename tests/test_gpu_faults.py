@@ -41,7 +41,7 @@ def test_selftest_wait_runs_out_and_context_survives(cuda):
     _tiny_check(cuda)
 
 
-@pytest.mark.parametrize("path", ["store", "kvi8r", "exact", "store_f8", "kvf8s", "store_fp4", "kvfp4"])
+@pytest.mark.parametrize("path", ["store", "kvi8r", "exact", "store_f8", "kvf8s", "store_fp4", "kvfp4", "hostio"])
 def test_kernels_give_up_under_tiny_wait_limit(cuda, path):
     b = _b()
     s = torch.cuda.current_stream().cuda_stream
@@ -50,6 +50,7 @@ def test_kernels_give_up_under_tiny_wait_limit(cuda, path):
     st = b.build_store(k, v)
     st8 = b.build_store_f8(k, v)
     st4 = b.build_store_fp4(k, v)
+    hq = q.cpu().contiguous().pin_memory()
     assert b.h3kv_sync_status(s) == b.H3KV_OK
     b.check(b.h3kv_set_wait_timeout_ns(1))
     try:
@@ -65,6 +66,9 @@ def test_kernels_give_up_under_tiny_wait_limit(cuda, path):
             b.build_store_fp4(k, v, out=st4)
         elif path == "kvfp4":
             b.attend_fp4(q, st4, q_chunk=4096, kv_block=0)
+        elif path == "hostio":
+            # four chunks: the chained launches' ready-word waits run under the limit too
+            b.attend_hostio(hq, st, q_chunk=1024, kv_block=0)
         else:
             b.attend_f8(q, st8, q_chunk=4096, kv_block=0)
         status = b.h3kv_sync_status(s)

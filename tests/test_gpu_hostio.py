@@ -2,7 +2,10 @@
 streamed through HBM one query chunk at a time (the q_chunk input bounds the
 device transient), with the copies of other chunks overlapping the attention
 of the current one.  Every chunk runs the same kernel with the same per-row
-arithmetic as h3kv_attend, so the outputs must be bit-identical."""
+arithmetic as h3kv_attend, so the outputs must be bit-identical.  Launches
+after the first wait inside the kernel for their buffer's ready word; the
+cases include many chunks (20, and 1100 one-row chunks, more than the ready
+values before they repeat)."""
 import pytest
 import torch
 
@@ -18,7 +21,8 @@ def _b():
 
 @pytest.mark.parametrize("heads,q_seq,kv_seq,q_chunk,kv_block",
                          [(1, 1024, 1024, 256, 512), (2, 1000, 1337, 300, 512), (3, 700, 900, 4096, 0),
-                          (1, 5, 300, 1, 128), (3, 4096, 2000, 1000, 1024), (2, 4100, 513, 2048, 256)])
+                          (1, 5, 300, 1, 128), (3, 4096, 2000, 1000, 1024), (2, 4100, 513, 2048, 256),
+                          (2, 5000, 2000, 256, 512), (1, 1100, 300, 1, 128)])
 def test_hostio_bit_identical_to_device_attend(cuda, heads, q_seq, kv_seq, q_chunk, kv_block):
     b = _b()
     q, k, v = synth.make_qkv(heads, kv_seq, seed=31, q_seq=q_seq, k_outliers=True)
