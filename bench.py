@@ -456,7 +456,7 @@ def run_ours(args, w, name):
     # ---- the same store held in pinned Grace memory and staged into HBM one
     # kv_block at a time (the pages keep kv_block for a host-staged K/V design)
     hst = b.Store.empty(H, L, host=True)
-    staging = torch.empty(int(b.h3kv_staging_bytes(H, kv_block)), dtype=torch.uint8, device=dev)
+    staging = torch.empty(b.staging_bytes_double(H, kv_block), dtype=torch.uint8, device=dev)
     state = torch.empty((H, L, 2), dtype=torch.float32, device=dev)
     b.build_store(k, v, out=hst)
     b.attend_staged(q, hst, q_chunk=q_chunk, kv_block=kv_block, out=out, staging=staging, state=state)

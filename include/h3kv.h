@@ -149,7 +149,13 @@ size_t h3kv_staging_bytes(int32_t heads, int32_t kv_block);
  * (scale_group 0 or 128; H3KV_ERR_UNSUPPORTED otherwise).  The library
  * allocates nothing:
  * staging and state are caller-owned scratch, reused by each call, so calls
- * that overlap on the GPU must not share them. */
+ * that overlap on the GPU must not share them.
+ * With staging_bytes >= round_up(h3kv_staging_bytes(...), 256) +
+ * h3kv_staging_bytes(...), two blocks are staged: the copy of block b + 1
+ * runs on a second stream (created for the call) while block b is attended.
+ * With less, each block's copy runs on `stream` between the blocks' launches.
+ * Within a block, the launches of successive query chunks follow each other
+ * as in h3kv_attend. */
 h3kv_status h3kv_attend_staged(const uint16_t *Q, int64_t q_seq, const h3kv_store *store, int32_t q_chunk,
                                int32_t kv_block, float softmax_scale, float *O, void *staging,
                                size_t staging_bytes, float *state, void *stream);

@@ -187,20 +187,29 @@ def attend(Q: torch.Tensor, store: Store, q_chunk: int = 16384, kv_block: int = 
     return out
 
 
+def staging_bytes_double(heads: int, kv_block: int) -> int:
+    """Staging bytes with room for two kv_blocks (h3kv_attend_staged then
+    copies the next block while attending the current one)."""
+    need = int(h3kv_staging_bytes(int(heads), int(kv_block)))
+    return (need + 255) // 256 * 256 + need
+
+
 def attend_staged(Q: torch.Tensor, store: Store, q_chunk: int = 16384, kv_block: int = 0,
                   softmax_scale: float = 0.0, out: torch.Tensor | None = None, staging: torch.Tensor | None = None,
                   state: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """h3kv_attend_staged: kvi8r attention over a store held outside HBM (e.g.
     ``Store.empty(..., host=True)``), staged through HBM one kv_block at a
-    time.  ``staging`` (uint8, >= h3kv_staging_bytes) and ``state`` (fp32
-    [heads, q_seq, 2]) are device scratch; they are created here if not
-    given."""
+    time.  ``staging`` (uint8, >= h3kv_staging_bytes; with
+    ``staging_bytes_double`` bytes two blocks are staged and the next block's
+    copy overlaps the current block's attention) and ``state`` (fp32 [heads,
+    q_seq, 2]) are device scratch; they are created here if not given (the
+    staging with room for two blocks)."""
     dev = Q.device
     heads, q_seq = int(Q.shape[0]), int(Q.shape[1])
     out = torch.empty(Q.shape, dtype=torch.float32, device=dev) if out is None else out
-    nbytes = int(h3kv_staging_bytes(store.heads, int(kv_block)))
     if staging is None:
-        staging = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+        staging = torch.empty(max(staging_bytes_double(store.heads, int(kv_block)), 16), dtype=torch.uint8,
+                              device=dev)
     if state is None:
         state = torch.empty((heads, q_seq, 2), dtype=torch.float32, device=dev)
     st = store.c_struct()

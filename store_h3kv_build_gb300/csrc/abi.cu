@@ -320,17 +320,24 @@ h3kv_status h3kv_attend_staged(const uint16_t *Q, int64_t q_seq, const h3kv_stor
   st = device_info(&d);
   if (st != H3KV_OK) return st;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // staging layout: k codes [H, kvb, 128], v codes, k scales [H, kvb], v scales
-  int8_t *skc = static_cast<int8_t *>(staging);
-  int8_t *svc = skc + H * kvb * 128;
-  uint16_t *sks = reinterpret_cast<uint16_t *>(svc + H * kvb * 128);
-  uint16_t *svs = sks + H * kvb;
+  // staging: one or two blocks, each k codes [H, kvb, 128], v codes, k
+  // scales [H, kvb], v scales; the second (if the scratch holds two) starts
+  // at the first block's size rounded up to 256 bytes
+  const size_t need = h3kv_staging_bytes(store->heads, static_cast<int32_t>(kvb));
+  const size_t need_aligned = (need + 255) & ~static_cast<size_t>(255);
+  const int nbuf = staging_bytes >= need_aligned + need ? 2 : 1;
+  struct StageBuf {
+    int8_t *kc, *vc;
+    uint16_t *ks, *vs;
+  } buf[2];
+  for (int p = 0; p < nbuf; ++p) {
+    buf[p].kc = static_cast<int8_t *>(staging) + p * need_aligned;
+    buf[p].vc = buf[p].kc + H * kvb * 128;
+    buf[p].ks = reinterpret_cast<uint16_t *>(buf[p].vc + H * kvb * 128);
+    buf[p].vs = buf[p].ks + H * kvb;
+  }
   h3kv::AttnArgs a{};
   a.q = Q;
-  a.k_codes = skc;
-  a.v_codes = svc;
-  a.k_scales = sks;
-  a.v_scales = svs;
   a.o = O;
   a.q_seq = q_seq;
   a.kv_stride = kvb;
@@ -341,31 +348,77 @@ h3kv_status h3kv_attend_staged(const uint16_t *Q, int64_t q_seq, const h3kv_stor
   a.state = reinterpret_cast<float2 *>(state);
   a.scale_groups = 1;
   const int64_t n_blocks = (store->seq + kvb - 1) / kvb;
-  for (int64_t b = 0; b < n_blocks; ++b) {
-    const int64_t b0 = b * kvb;
-    const int64_t len = store->seq - b0 < kvb ? store->seq - b0 : kvb;
-    // one block of every head into the staging buffer (stream-ordered after
-    // the previous block's launches, which read the same buffer)
-    if (cudaMemcpy2DAsync(skc, kvb * 128, store->k_codes + b0 * 128, store->seq * 128, len * 128, H,
-                          cudaMemcpyDefault, s) != cudaSuccess ||
-        cudaMemcpy2DAsync(svc, kvb * 128, store->v_codes + b0 * 128, store->seq * 128, len * 128, H,
-                          cudaMemcpyDefault, s) != cudaSuccess ||
-        cudaMemcpy2DAsync(sks, kvb * 2, store->k_scales + b0, store->seq * 2, len * 2, H, cudaMemcpyDefault,
-                          s) != cudaSuccess ||
-        cudaMemcpy2DAsync(svs, kvb * 2, store->v_scales + b0, store->seq * 2, len * 2, H, cudaMemcpyDefault,
-                          s) != cudaSuccess)
-      return H3KV_ERR_CUDA;
+  auto len_of = [&](int64_t b) { return store->seq - b * kvb < kvb ? store->seq - b * kvb : kvb; };
+  // one block of every head into staging buffer p, on stream cs
+  auto copy_block = [&](int64_t b, int p, cudaStream_t cs) {
+    const int64_t b0 = b * kvb, len = len_of(b);
+    return cudaMemcpy2DAsync(buf[p].kc, kvb * 128, store->k_codes + b0 * 128, store->seq * 128, len * 128, H,
+                             cudaMemcpyDefault, cs) == cudaSuccess &&
+           cudaMemcpy2DAsync(buf[p].vc, kvb * 128, store->v_codes + b0 * 128, store->seq * 128, len * 128, H,
+                             cudaMemcpyDefault, cs) == cudaSuccess &&
+           cudaMemcpy2DAsync(buf[p].ks, kvb * 2, store->k_scales + b0, store->seq * 2, len * 2, H,
+                             cudaMemcpyDefault, cs) == cudaSuccess &&
+           cudaMemcpy2DAsync(buf[p].vs, kvb * 2, store->v_scales + b0, store->seq * 2, len * 2, H,
+                             cudaMemcpyDefault, cs) == cudaSuccess;
+  };
+  // Every query chunk of block b over buffer p.  Launches after a block's
+  // first follow the previous one with programmatic dependent launch: they
+  // touch other query rows and only read the staged block.  A block's first
+  // launch is a plain one, after everything before it in the stream, so the
+  // state and O rows that the previous block's launches carry are complete
+  // (each launch completes only after the one before it).
+  auto attend_block = [&](int64_t b, int p) {
+    const int64_t len = len_of(b);
+    a.k_codes = buf[p].kc;
+    a.v_codes = buf[p].vc;
+    a.k_scales = buf[p].ks;
+    a.v_scales = buf[p].vs;
     a.kv_seq = len;
     a.kv_block_tiles = static_cast<int32_t>((len + H3KV_KV_TILE - 1) / H3KV_KV_TILE);
     a.stage_flags = (b == 0 ? 1 : 0) | (b == n_blocks - 1 ? 2 : 0);
     for (int64_t c0 = 0; c0 < q_seq; c0 += q_chunk) {
       a.q_begin = c0;
       a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
-      // staged launches carry state from block to block: never overlapped
-      if (h3kv::launch_attend_kvi8r(a, false, s) != cudaSuccess) return H3KV_ERR_CUDA;
+      if (h3kv::launch_attend_kvi8r(a, c0 > 0, s) != cudaSuccess) return false;
     }
+    return true;
+  };
+  if (nbuf == 1) {
+    // each block's copy is stream-ordered after the previous block's
+    // launches, which read the same buffer
+    for (int64_t b = 0; b < n_blocks; ++b)
+      if (!copy_block(b, 0, s) || !attend_block(b, 0)) return H3KV_ERR_CUDA;
+    return H3KV_OK;
   }
-  return H3KV_OK;
+  // Two buffers: block b + 1 is copied on a second stream while block b is
+  // attended; the copy into buffer p waits for the launches of block b - 2,
+  // the last ones to read it, and block b's launches wait for its copy.
+  cudaStream_t cs = nullptr;
+  cudaEvent_t entry = nullptr, copied[2] = {nullptr, nullptr}, done[2] = {nullptr, nullptr};
+  h3kv_status result = H3KV_OK;
+  const unsigned ef = cudaEventDisableTiming;
+  bool ok = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&entry, ef) == cudaSuccess &&
+            cudaEventCreateWithFlags(&copied[0], ef) == cudaSuccess &&
+            cudaEventCreateWithFlags(&copied[1], ef) == cudaSuccess &&
+            cudaEventCreateWithFlags(&done[0], ef) == cudaSuccess &&
+            cudaEventCreateWithFlags(&done[1], ef) == cudaSuccess;
+  // the copies start after everything queued on the caller's stream (which
+  // may have written the store)
+  ok = ok && cudaEventRecord(entry, s) == cudaSuccess && cudaStreamWaitEvent(cs, entry, 0) == cudaSuccess;
+  for (int64_t b = 0; ok && b < n_blocks; ++b) {
+    const int p = static_cast<int>(b & 1);
+    ok = (b < 2 || cudaStreamWaitEvent(cs, done[p], 0) == cudaSuccess) && copy_block(b, p, cs) &&
+         cudaEventRecord(copied[p], cs) == cudaSuccess && cudaStreamWaitEvent(s, copied[p], 0) == cudaSuccess &&
+         attend_block(b, p) && cudaEventRecord(done[p], s) == cudaSuccess;
+  }
+  if (!ok) result = H3KV_ERR_CUDA;
+  // (every copy on cs is waited on by a launch on s, so later work on s is
+  // ordered after all of them)
+  for (cudaEvent_t e : {entry, copied[0], copied[1], done[0], done[1]})
+    if (e) cudaEventDestroy(e);
+  if (cs) cudaStreamDestroy(cs);
+  return result;
 }
 
 size_t h3kv_hostio_scratch_bytes(int32_t heads, int32_t q_chunk) {

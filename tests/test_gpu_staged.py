@@ -29,16 +29,22 @@ def _b():
     (3, 129, 5, 64, 128),           # one block shorter than a tile
     (1, 4096, 4096, 4096, 0),       # kv_block 16384 > sequence: one block
     (2, 700, 3000, 256, 1024),      # three blocks, last one ragged
+    (2, 2100, 5000, 512, 512),      # ten blocks of five query chunks each
 ])
-def test_staged_bit_identical_to_resident(cuda, heads, q_seq, kv_seq, q_chunk, kv_block):
+@pytest.mark.parametrize("buffers", [1, 2])
+def test_staged_bit_identical_to_resident(cuda, heads, q_seq, kv_seq, q_chunk, kv_block, buffers):
+    # buffers 1: each block copied on the caller's stream between the blocks'
+    # launches; 2: the next block copied on a second stream meanwhile
     b = _b()
     q, k, v = synth.make_qkv(heads, kv_seq, seed=31, q_seq=q_seq, k_outliers=True)
     qd = q.to(cuda)
     dev = b.build_store(k.to(cuda), v.to(cuda))
     host = b.build_store(k.to(cuda), v.to(cuda), out=b.Store.empty(heads, kv_seq, host=True))
     ref = b.attend(qd, dev, q_chunk=q_chunk, kv_block=kv_block)
-    staged_host = b.attend_staged(qd, host, q_chunk=q_chunk, kv_block=kv_block)
-    staged_dev = b.attend_staged(qd, dev, q_chunk=q_chunk, kv_block=kv_block)
+    nbytes = b.h3kv_staging_bytes(heads, kv_block) if buffers == 1 else b.staging_bytes_double(heads, kv_block)
+    staging = torch.empty(nbytes, dtype=torch.uint8, device=cuda)
+    staged_host = b.attend_staged(qd, host, q_chunk=q_chunk, kv_block=kv_block, staging=staging)
+    staged_dev = b.attend_staged(qd, dev, q_chunk=q_chunk, kv_block=kv_block, staging=staging)
     b.sync_status()
     assert torch.equal(staged_host, ref)
     assert torch.equal(staged_dev, ref)
@@ -60,3 +66,26 @@ def test_staged_reuses_scratch_across_calls(cuda):
     b.sync_status()
     assert torch.equal(outs[0], outs[2])
     assert not torch.equal(outs[0], outs[1])
+
+
+def test_staged_double_buffer_on_a_side_stream(cuda):
+    # two calls on a side stream sharing one two-block staging buffer, with the
+    # store written on that stream just before: the copies stream is ordered
+    # after earlier work on the stream, and later work sees every output row
+    b = _b()
+    heads, seq, kvb = 2, 3000, 256
+    q, k, v = synth.make_qkv(heads, seq, seed=43, k_outliers=True)
+    qd, kd, vd = q.to(cuda), k.to(cuda), v.to(cuda)
+    ref = b.attend(qd, b.build_store(kd, vd), q_chunk=1000, kv_block=kvb)
+    host = b.Store.empty(heads, seq, host=True)
+    staging = torch.empty(b.staging_bytes_double(heads, kvb), dtype=torch.uint8, device=cuda)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        b.build_store(kd, vd, out=host, stream=side)
+        o1 = b.attend_staged(qd, host, q_chunk=1000, kv_block=kvb, staging=staging, stream=side)
+        o2 = b.attend_staged(qd, host, q_chunk=1000, kv_block=kvb, staging=staging, stream=side)
+        s1, s2 = o1.sum(), o2.sum()
+    b.sync_status(side)
+    assert torch.equal(o1, ref) and torch.equal(o2, ref)
+    assert float(s1) == float(s2)
