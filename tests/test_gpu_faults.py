@@ -41,7 +41,7 @@ def test_selftest_wait_runs_out_and_context_survives(cuda):
     _tiny_check(cuda)
 
 
-@pytest.mark.parametrize("path", ["store", "kvi8r", "exact", "store_f8", "kvf8s", "store_fp4", "kvfp4", "hostio"])
+@pytest.mark.parametrize("path", ["store", "kvi8r", "exact", "store_f8", "kvf8s", "store_fp4", "kvfp4", "hostio", "staged"])
 def test_kernels_give_up_under_tiny_wait_limit(cuda, path):
     b = _b()
     s = torch.cuda.current_stream().cuda_stream
@@ -69,6 +69,9 @@ def test_kernels_give_up_under_tiny_wait_limit(cuda, path):
         elif path == "hostio":
             # four chunks: the chained launches' ready-word waits run under the limit too
             b.attend_hostio(hq, st, q_chunk=1024, kv_block=0)
+        elif path == "staged":
+            # four blocks through two staging buffers: the blocks' ready-word waits too
+            b.attend_staged(q, st, q_chunk=2048, kv_block=1024)
         else:
             b.attend_f8(q, st8, q_chunk=4096, kv_block=0)
         status = b.h3kv_sync_status(s)
