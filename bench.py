@@ -514,7 +514,8 @@ def run_ours(args, w, name):
                           "build_frac_of_hbm": fp4_bytes / (fp4_build_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
                           "store_bytes": 2 * H * L * (64 + 8)},
             "host_store": {"where": "kvi8r store built into pinned Grace memory over NVLink-C2C, attended "
-                                    "with h3kv_attend_staged (each kv_block copied into HBM, copies timed)",
+                                    "with h3kv_attend_staged (each kv_block copied into HBM through two staging "
+                                    "blocks, the next copy overlapping the current block; copies timed)",
                            "attend_ms": host_attend_ms, "attend_tflops": flops / (host_attend_ms / 1e3) / 1e12,
                            "build_ms": host_build_ms,
                            "build_gbs": store_bytes(H, L) / (host_build_ms / 1e3) / 1e9},
