@@ -9,8 +9,8 @@ if ROOT not in sys.path:
 
 
 def _ensure_library():
-    """Build libh3kv.so in-tree if it is missing (nvcc cross-compiles here and
-    on the GPU machine alike), so the binding never silently falls back."""
+    """Build libh3kv.so in-tree if it is missing (nvcc compiles it for sm_103a
+    with or without a GPU present), so the binding never silently falls back."""
     lib = os.path.join(ROOT, "store_h3kv_build_gb300", "libh3kv.so")
     if not os.path.exists(lib):
         from store_h3kv_build_gb300 import build_lib
