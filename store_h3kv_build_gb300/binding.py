@@ -8,6 +8,7 @@ module loads the library and raises ImportError if it has not been built
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -123,6 +124,14 @@ def _stream(stream=None) -> int:
     return s.cuda_stream
 
 
+def _on(stream=None):
+    """Context for the device tensors the binding allocates for a call
+    (outputs, stores, scratch): the call's stream, so that PyTorch's caching
+    allocator hands a freed block to new work only after that stream's work
+    on it -- a scratch dropped when the call returns is still in use there."""
+    return torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext()
+
+
 class Store:
     """A kvi8r store held in torch tensors: int8 codes [heads, seq, 128] and
     fp16 scales [heads, seq] for K and for V."""
@@ -168,7 +177,8 @@ def build_store(K: torch.Tensor, V: torch.Tensor, out: Store | None = None, stre
     """h3kv_build_store on bf16 K, V [heads, seq, 128] (CUDA, contiguous);
     scale_group 32 gives one scale per 32 rotated values."""
     heads, seq = int(K.shape[0]), int(K.shape[1])
-    out = Store.empty(heads, seq, K.device, scale_group=scale_group) if out is None else out
+    with _on(stream):
+        out = Store.empty(heads, seq, K.device, scale_group=scale_group) if out is None else out
     st = out.c_struct()
     check(h3kv_build_store(_ptr(K), _ptr(V), heads, seq, int(K.shape[2]), ctypes.byref(st), _stream(stream)),
           "h3kv_build_store")
@@ -180,7 +190,8 @@ def attend(Q: torch.Tensor, store: Store, q_chunk: int = 16384, kv_block: int = 
     """h3kv_attend: kvi8r attention of bf16 Q [heads, q_seq, 128] over `store`
     -> fp32 [heads, q_seq, 128]."""
     q_seq = int(Q.shape[1])
-    out = torch.empty(Q.shape, dtype=torch.float32, device=Q.device) if out is None else out
+    with _on(stream):
+        out = torch.empty(Q.shape, dtype=torch.float32, device=Q.device) if out is None else out
     st = store.c_struct()
     check(h3kv_attend(_ptr(Q), q_seq, ctypes.byref(st), int(q_chunk), int(kv_block), float(softmax_scale),
                       _ptr(out), _stream(stream)), "h3kv_attend")
@@ -206,12 +217,13 @@ def attend_staged(Q: torch.Tensor, store: Store, q_chunk: int = 16384, kv_block:
     staging with room for two blocks)."""
     dev = Q.device
     heads, q_seq = int(Q.shape[0]), int(Q.shape[1])
-    out = torch.empty(Q.shape, dtype=torch.float32, device=dev) if out is None else out
-    if staging is None:
-        staging = torch.empty(max(staging_bytes_double(store.heads, int(kv_block)), 16), dtype=torch.uint8,
-                              device=dev)
-    if state is None:
-        state = torch.empty((heads, q_seq, 2), dtype=torch.float32, device=dev)
+    with _on(stream):
+        out = torch.empty(Q.shape, dtype=torch.float32, device=dev) if out is None else out
+        if staging is None:
+            staging = torch.empty(max(staging_bytes_double(store.heads, int(kv_block)), 16), dtype=torch.uint8,
+                                  device=dev)
+        if state is None:
+            state = torch.empty((heads, q_seq, 2), dtype=torch.float32, device=dev)
     st = store.c_struct()
     check(h3kv_attend_staged(_ptr(Q), q_seq, ctypes.byref(st), int(q_chunk), int(kv_block), float(softmax_scale),
                              _ptr(out), _ptr(staging), staging.numel() * staging.element_size(), _ptr(state),
@@ -232,8 +244,9 @@ def attend_hostio(Q_host: torch.Tensor, store: Store, q_chunk: int = 16384, kv_b
         out = torch.empty(Q_host.shape, dtype=torch.float32, pin_memory=True)
     if scratch is None:
         dev = store.k_codes.device
-        scratch = torch.empty(max(int(h3kv_hostio_scratch_bytes(heads, int(q_chunk))), 16), dtype=torch.uint8,
-                              device=dev)
+        with _on(stream):
+            scratch = torch.empty(max(int(h3kv_hostio_scratch_bytes(heads, int(q_chunk))), 16), dtype=torch.uint8,
+                                  device=dev)
     st = store.c_struct()
     check(h3kv_attend_hostio(_ptr(Q_host), q_seq, ctypes.byref(st), int(q_chunk), int(kv_block),
                              float(softmax_scale), _ptr(out), _ptr(scratch), scratch.numel(), _stream(stream)),
@@ -244,7 +257,8 @@ def attend_hostio(Q_host: torch.Tensor, store: Store, q_chunk: int = 16384, kv_b
 def attend_exact(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, q_chunk: int = 16384, kv_block: int = 0,
                  softmax_scale: float = 0.0, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """h3kv_attend_exact: softmax attention on bf16 Q, K, V -> fp32."""
-    out = torch.empty(Q.shape, dtype=torch.float32, device=Q.device) if out is None else out
+    with _on(stream):
+        out = torch.empty(Q.shape, dtype=torch.float32, device=Q.device) if out is None else out
     check(h3kv_attend_exact(_ptr(Q), int(Q.shape[1]), _ptr(K), _ptr(V), int(K.shape[0]), int(K.shape[1]),
                             int(K.shape[2]), int(q_chunk), int(kv_block), float(softmax_scale), _ptr(out),
                             _stream(stream)), "h3kv_attend_exact")
@@ -287,7 +301,8 @@ class StoreF8:
 def build_store_f8(K: torch.Tensor, V: torch.Tensor, out: StoreF8 | None = None, stream=None) -> StoreF8:
     """h3kv_build_store_f8 on bf16 K, V [heads, seq, 128] (CUDA, contiguous)."""
     heads, seq = int(K.shape[0]), int(K.shape[1])
-    out = StoreF8.empty(heads, seq, K.device) if out is None else out
+    with _on(stream):
+        out = StoreF8.empty(heads, seq, K.device) if out is None else out
     st = out.c_struct()
     check(h3kv_build_store_f8(_ptr(K), _ptr(V), heads, seq, int(K.shape[2]), ctypes.byref(st), _stream(stream)),
           "h3kv_build_store_f8")
@@ -298,7 +313,8 @@ def attend_f8(Q: torch.Tensor, store: StoreF8, q_chunk: int = 16384, kv_block: i
               out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """h3kv_attend_f8: kvf8s attention of bf16 Q [heads, q_seq, 128] -> fp32."""
     q_seq = int(Q.shape[1])
-    out = torch.empty(Q.shape, dtype=torch.float32, device=Q.device) if out is None else out
+    with _on(stream):
+        out = torch.empty(Q.shape, dtype=torch.float32, device=Q.device) if out is None else out
     st = store.c_struct()
     check(h3kv_attend_f8(_ptr(Q), q_seq, ctypes.byref(st), int(q_chunk), int(kv_block), float(softmax_scale),
                          _ptr(out), _stream(stream)), "h3kv_attend_f8")
@@ -332,7 +348,8 @@ class StoreFp4:
 def build_store_fp4(K: torch.Tensor, V: torch.Tensor, out: StoreFp4 | None = None, stream=None) -> StoreFp4:
     """h3kv_build_store_fp4 on bf16 K, V [heads, seq, 128] (CUDA, contiguous)."""
     heads, seq = int(K.shape[0]), int(K.shape[1])
-    out = StoreFp4.empty(heads, seq, K.device) if out is None else out
+    with _on(stream):
+        out = StoreFp4.empty(heads, seq, K.device) if out is None else out
     st = out.c_struct()
     check(h3kv_build_store_fp4(_ptr(K), _ptr(V), heads, seq, int(K.shape[2]), ctypes.byref(st), _stream(stream)),
           "h3kv_build_store_fp4")
@@ -343,7 +360,8 @@ def attend_fp4(Q: torch.Tensor, store: StoreFp4, q_chunk: int = 16384, kv_block:
                softmax_scale: float = 0.0, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """h3kv_attend_fp4: kvfp4 attention of bf16 Q [heads, q_seq, 128] -> fp32."""
     q_seq = int(Q.shape[1])
-    out = torch.empty(Q.shape, dtype=torch.float32, device=Q.device) if out is None else out
+    with _on(stream):
+        out = torch.empty(Q.shape, dtype=torch.float32, device=Q.device) if out is None else out
     st = store.c_struct()
     check(h3kv_attend_fp4(_ptr(Q), q_seq, ctypes.byref(st), int(q_chunk), int(kv_block), float(softmax_scale),
                           _ptr(out), _stream(stream)), "h3kv_attend_fp4")

@@ -50,3 +50,25 @@ def test_hostio_reuses_scratch_and_orders_on_stream(cuda):
         o2 = b.attend_hostio(hq, st, q_chunk=512, kv_block=1024, scratch=scratch, stream=side)
     b.sync_status(side)
     assert torch.equal(o1, ref) and torch.equal(o2, ref)
+
+
+def test_hostio_calls_on_two_streams_at_once(cuda):
+    # two calls in flight together, each with its own scratch (the pinned
+    # value table behind the ready words is shared and read-only), many
+    # chunks each: both outputs bit-identical to device attention
+    b = _b()
+    heads, q_seq, kv_seq, q_chunk = 2, 3000, 1500, 256
+    q1, k, v = synth.make_qkv(heads, kv_seq, seed=51, q_seq=q_seq, k_outliers=True)
+    q2 = synth.normal_bf16((heads, q_seq, 128), 52)
+    st = b.build_store(k.to(cuda), v.to(cuda))
+    ref1 = b.attend(q1.to(cuda), st, q_chunk=q_chunk, kv_block=512).cpu()
+    ref2 = b.attend(q2.to(cuda), st, q_chunk=q_chunk, kv_block=512).cpu()
+    h1, h2 = q1.contiguous().pin_memory(), q2.contiguous().pin_memory()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    s1.wait_stream(torch.cuda.current_stream())
+    s2.wait_stream(torch.cuda.current_stream())
+    o1 = b.attend_hostio(h1, st, q_chunk=q_chunk, kv_block=512, stream=s1)
+    o2 = b.attend_hostio(h2, st, q_chunk=q_chunk, kv_block=512, stream=s2)
+    b.sync_status(s1)
+    b.sync_status(s2)
+    assert torch.equal(o1, ref1) and torch.equal(o2, ref2)
