@@ -89,3 +89,29 @@ def test_staged_double_buffer_on_a_side_stream(cuda):
     b.sync_status(side)
     assert torch.equal(o1, ref) and torch.equal(o2, ref)
     assert float(s1) == float(s2)
+
+
+def test_staged_calls_on_two_streams_at_once(cuda):
+    # two calls in flight together over one store in Grace memory, each with
+    # the staging and state the binding creates for it (two staging blocks,
+    # a copy stream per call): both outputs bit-identical to the resident path
+    b = _b()
+    heads, seq, kvb = 2, 3000, 256
+    q1, k, v = synth.make_qkv(heads, seq, seed=44, k_outliers=True)
+    q2 = synth.normal_bf16((heads, seq, 128), 45)
+    kd, vd = k.to(cuda), v.to(cuda)
+    dev = b.build_store(kd, vd)
+    host = b.build_store(kd, vd, out=b.Store.empty(heads, seq, host=True))
+    ref1 = b.attend(q1.to(cuda), dev, q_chunk=1000, kv_block=kvb)
+    ref2 = b.attend(q2.to(cuda), dev, q_chunk=1000, kv_block=kvb)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    s1.wait_stream(torch.cuda.current_stream())
+    s2.wait_stream(torch.cuda.current_stream())
+    qa, qb = q1.to(cuda), q2.to(cuda)
+    s1.wait_stream(torch.cuda.current_stream())
+    s2.wait_stream(torch.cuda.current_stream())
+    o1 = b.attend_staged(qa, host, q_chunk=1000, kv_block=kvb, stream=s1)
+    o2 = b.attend_staged(qb, host, q_chunk=1000, kv_block=kvb, stream=s2)
+    b.sync_status(s1)
+    b.sync_status(s2)
+    assert torch.equal(o1, ref1) and torch.equal(o2, ref2)
