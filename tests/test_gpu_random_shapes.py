@@ -62,3 +62,31 @@ def test_random_shape_every_path(cuda, heads, q_seq, kv_seq, q_chunk, kv_block, 
         o = b.attend_f8(qd, st8, q_chunk=q_chunk, kv_block=kv_block)
         b.sync_status()
         compare_f8_attention(o, q, f8_store_numpy(st8), "kvf8s " + what)
+
+
+def test_four_paths_on_four_streams_at_once(cuda):
+    # kvi8r, exact, kvfp4 and kvf8s attention in flight together on four
+    # streams, each a chain of query-chunk launches (programmatic dependent
+    # launch within each stream): every output bit-identical to the same
+    # call run alone
+    from store_h3kv_build_gb300 import binding as b
+    heads, seq, q_chunk, kvb = 3, 2500, 512, 1024
+    q, k, v = synth.make_qkv(heads, seq, seed=61, k_outliers=True)
+    qd, kd, vd = q.to(cuda), k.to(cuda), v.to(cuda)
+    st, st4, st8 = b.build_store(kd, vd), b.build_store_fp4(kd, vd), b.build_store_f8(kd, vd)
+    calls = [
+        lambda s: b.attend(qd, st, q_chunk=q_chunk, kv_block=kvb, stream=s),
+        lambda s: b.attend_exact(qd, kd, vd, q_chunk=q_chunk, kv_block=kvb, stream=s),
+        lambda s: b.attend_fp4(qd, st4, q_chunk=q_chunk, kv_block=kvb, stream=s),
+        lambda s: b.attend_f8(qd, st8, q_chunk=q_chunk, kv_block=kvb, stream=s),
+    ]
+    refs = [c(None) for c in calls]
+    b.sync_status()
+    streams = [torch.cuda.Stream() for _ in calls]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    outs = [c(s) for c, s in zip(calls, streams)]
+    for s in streams:
+        b.sync_status(s)
+    for name, o, r in zip(("kvi8r", "exact", "kvfp4", "kvf8s"), outs, refs):
+        assert torch.equal(o, r), name
