@@ -119,6 +119,33 @@ def _ptr(t) -> int:
     return 0 if t is None else t.data_ptr()
 
 
+def _need(t, name: str, dtype, shape=None) -> None:
+    """Argument check: the library reads and writes raw contiguous buffers of
+    the sizes its arguments imply, so a strided view, another dtype or a
+    buffer of another shape would be read as garbage or written past its end."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(int(x) for x in shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(int(x) for x in shape)}")
+
+
+def _need_rows(t, name: str, heads: int | None = None) -> None:
+    """bf16 [heads, rows, 128] input (Q, K or V)."""
+    _need(t, name, torch.bfloat16)
+    if t.dim() != 3 or t.shape[2] != HEAD_DIM:
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected [heads, rows, {HEAD_DIM}]")
+    if heads is not None and t.shape[0] != heads:
+        raise ValueError(f"{name}: {t.shape[0]} heads, the store has {heads}")
+
+
+def _need_out(out, Q) -> None:
+    _need(out, "out", torch.float32, Q.shape)
+
+
 def _stream(stream=None) -> int:
     s = torch.cuda.current_stream() if stream is None else stream
     return s.cuda_stream
@@ -165,6 +192,12 @@ class Store:
         return not self.k_codes.is_cuda
 
     def c_struct(self) -> h3kv_store:
+        H, L = self.heads, self.seq
+        _need(self.k_codes, "store.k_codes", torch.int8, (H, L, HEAD_DIM))
+        _need(self.v_codes, "store.v_codes", torch.int8, (H, L, HEAD_DIM))
+        sshape = (H, L, HEAD_DIM // 32) if self.scale_group == 32 else (H, L)
+        _need(self.k_scales, "store.k_scales", torch.float16, sshape)
+        _need(self.v_scales, "store.v_scales", torch.float16, sshape)
         return h3kv_store(_ptr(self.k_codes), _ptr(self.v_codes), _ptr(self.k_scales), _ptr(self.v_scales),
                           self.heads, self.seq, HEAD_DIM, self.scale_group)
 
@@ -176,6 +209,10 @@ def build_store(K: torch.Tensor, V: torch.Tensor, out: Store | None = None, stre
                 scale_group: int = 0) -> Store:
     """h3kv_build_store on bf16 K, V [heads, seq, 128] (CUDA, contiguous);
     scale_group 32 gives one scale per 32 rotated values."""
+    _need_rows(K, "K")
+    _need_rows(V, "V")
+    if V.shape != K.shape:
+        raise ValueError(f"V: shape {tuple(V.shape)}, K has {tuple(K.shape)}")
     heads, seq = int(K.shape[0]), int(K.shape[1])
     with _on(stream):
         out = Store.empty(heads, seq, K.device, scale_group=scale_group) if out is None else out
@@ -189,9 +226,11 @@ def attend(Q: torch.Tensor, store: Store, q_chunk: int = 16384, kv_block: int = 
            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """h3kv_attend: kvi8r attention of bf16 Q [heads, q_seq, 128] over `store`
     -> fp32 [heads, q_seq, 128]."""
+    _need_rows(Q, "Q", store.heads)
     q_seq = int(Q.shape[1])
     with _on(stream):
         out = torch.empty(Q.shape, dtype=torch.float32, device=Q.device) if out is None else out
+    _need_out(out, Q)
     st = store.c_struct()
     check(h3kv_attend(_ptr(Q), q_seq, ctypes.byref(st), int(q_chunk), int(kv_block), float(softmax_scale),
                       _ptr(out), _stream(stream)), "h3kv_attend")
@@ -215,6 +254,7 @@ def attend_staged(Q: torch.Tensor, store: Store, q_chunk: int = 16384, kv_block:
     copy overlaps the current block's attention) and ``state`` (fp32 [heads,
     q_seq, 2]) are device scratch; they are created here if not given (the
     staging with room for two blocks)."""
+    _need_rows(Q, "Q", store.heads)
     dev = Q.device
     heads, q_seq = int(Q.shape[0]), int(Q.shape[1])
     with _on(stream):
@@ -224,6 +264,9 @@ def attend_staged(Q: torch.Tensor, store: Store, q_chunk: int = 16384, kv_block:
                                   device=dev)
         if state is None:
             state = torch.empty((heads, q_seq, 2), dtype=torch.float32, device=dev)
+    _need_out(out, Q)
+    _need(staging, "staging", torch.uint8)
+    _need(state, "state", torch.float32, (int(Q.shape[0]), int(Q.shape[1]), 2))
     st = store.c_struct()
     check(h3kv_attend_staged(_ptr(Q), q_seq, ctypes.byref(st), int(q_chunk), int(kv_block), float(softmax_scale),
                              _ptr(out), _ptr(staging), staging.numel() * staging.element_size(), _ptr(state),
@@ -239,6 +282,7 @@ def attend_hostio(Q_host: torch.Tensor, store: Store, q_chunk: int = 16384, kv_b
     output lands in host memory (``out``, pinned, created here if not
     given).  ``scratch`` (uint8 device, >= h3kv_hostio_scratch_bytes) is
     created here if not given."""
+    _need_rows(Q_host, "Q_host", store.heads)
     heads, q_seq = int(Q_host.shape[0]), int(Q_host.shape[1])
     if out is None:
         out = torch.empty(Q_host.shape, dtype=torch.float32, pin_memory=True)
@@ -247,6 +291,8 @@ def attend_hostio(Q_host: torch.Tensor, store: Store, q_chunk: int = 16384, kv_b
         with _on(stream):
             scratch = torch.empty(max(int(h3kv_hostio_scratch_bytes(heads, int(q_chunk))), 16), dtype=torch.uint8,
                                   device=dev)
+    _need_out(out, Q_host)
+    _need(scratch, "scratch", torch.uint8)
     st = store.c_struct()
     check(h3kv_attend_hostio(_ptr(Q_host), q_seq, ctypes.byref(st), int(q_chunk), int(kv_block),
                              float(softmax_scale), _ptr(out), _ptr(scratch), scratch.numel(), _stream(stream)),
@@ -257,8 +303,14 @@ def attend_hostio(Q_host: torch.Tensor, store: Store, q_chunk: int = 16384, kv_b
 def attend_exact(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, q_chunk: int = 16384, kv_block: int = 0,
                  softmax_scale: float = 0.0, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """h3kv_attend_exact: softmax attention on bf16 Q, K, V -> fp32."""
+    _need_rows(K, "K")
+    _need_rows(V, "V")
+    if V.shape != K.shape:
+        raise ValueError(f"V: shape {tuple(V.shape)}, K has {tuple(K.shape)}")
+    _need_rows(Q, "Q", int(K.shape[0]))
     with _on(stream):
         out = torch.empty(Q.shape, dtype=torch.float32, device=Q.device) if out is None else out
+    _need_out(out, Q)
     check(h3kv_attend_exact(_ptr(Q), int(Q.shape[1]), _ptr(K), _ptr(V), int(K.shape[0]), int(K.shape[1]),
                             int(K.shape[2]), int(q_chunk), int(kv_block), float(softmax_scale), _ptr(out),
                             _stream(stream)), "h3kv_attend_exact")
@@ -291,6 +343,12 @@ class StoreF8:
         return cls(kc, vt, ks, vs, km, seq)
 
     def c_struct(self) -> h3kv_store_f8:
+        H, L = self.heads, self.seq
+        _need(self.k_codes, "store.k_codes", torch.uint8, (H, L, HEAD_DIM))
+        _need(self.v_codes_t, "store.v_codes_t", torch.uint8, (H, HEAD_DIM, int(h3kv_f8_v_stride(L))))
+        _need(self.k_scales, "store.k_scales", torch.float32, (H, (L + K_BLOCK_F8 - 1) // K_BLOCK_F8))
+        _need(self.v_scales, "store.v_scales", torch.float32, (H, HEAD_DIM))
+        _need(self.k_mean, "store.k_mean", torch.float32, (H, HEAD_DIM))
         return h3kv_store_f8(_ptr(self.k_codes), _ptr(self.v_codes_t), _ptr(self.k_scales), _ptr(self.v_scales),
                              _ptr(self.k_mean), self.heads, self.seq, HEAD_DIM)
 
@@ -300,6 +358,10 @@ class StoreF8:
 
 def build_store_f8(K: torch.Tensor, V: torch.Tensor, out: StoreF8 | None = None, stream=None) -> StoreF8:
     """h3kv_build_store_f8 on bf16 K, V [heads, seq, 128] (CUDA, contiguous)."""
+    _need_rows(K, "K")
+    _need_rows(V, "V")
+    if V.shape != K.shape:
+        raise ValueError(f"V: shape {tuple(V.shape)}, K has {tuple(K.shape)}")
     heads, seq = int(K.shape[0]), int(K.shape[1])
     with _on(stream):
         out = StoreF8.empty(heads, seq, K.device) if out is None else out
@@ -312,9 +374,11 @@ def build_store_f8(K: torch.Tensor, V: torch.Tensor, out: StoreF8 | None = None,
 def attend_f8(Q: torch.Tensor, store: StoreF8, q_chunk: int = 16384, kv_block: int = 0, softmax_scale: float = 0.0,
               out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """h3kv_attend_f8: kvf8s attention of bf16 Q [heads, q_seq, 128] -> fp32."""
+    _need_rows(Q, "Q", store.heads)
     q_seq = int(Q.shape[1])
     with _on(stream):
         out = torch.empty(Q.shape, dtype=torch.float32, device=Q.device) if out is None else out
+    _need_out(out, Q)
     st = store.c_struct()
     check(h3kv_attend_f8(_ptr(Q), q_seq, ctypes.byref(st), int(q_chunk), int(kv_block), float(softmax_scale),
                          _ptr(out), _stream(stream)), "h3kv_attend_f8")
@@ -338,6 +402,11 @@ class StoreFp4:
         return cls(kc, torch.empty_like(kc), ks, torch.empty_like(ks))
 
     def c_struct(self) -> h3kv_store_fp4:
+        H, L = self.heads, self.seq
+        _need(self.k_codes, "store.k_codes", torch.uint8, (H, L, HEAD_DIM // 2))
+        _need(self.v_codes, "store.v_codes", torch.uint8, (H, L, HEAD_DIM // 2))
+        _need(self.k_scales, "store.k_scales", torch.uint8, (H, L, HEAD_DIM // 16))
+        _need(self.v_scales, "store.v_scales", torch.uint8, (H, L, HEAD_DIM // 16))
         return h3kv_store_fp4(_ptr(self.k_codes), _ptr(self.v_codes), _ptr(self.k_scales), _ptr(self.v_scales),
                               self.heads, self.seq, HEAD_DIM)
 
@@ -347,6 +416,10 @@ class StoreFp4:
 
 def build_store_fp4(K: torch.Tensor, V: torch.Tensor, out: StoreFp4 | None = None, stream=None) -> StoreFp4:
     """h3kv_build_store_fp4 on bf16 K, V [heads, seq, 128] (CUDA, contiguous)."""
+    _need_rows(K, "K")
+    _need_rows(V, "V")
+    if V.shape != K.shape:
+        raise ValueError(f"V: shape {tuple(V.shape)}, K has {tuple(K.shape)}")
     heads, seq = int(K.shape[0]), int(K.shape[1])
     with _on(stream):
         out = StoreFp4.empty(heads, seq, K.device) if out is None else out
@@ -359,9 +432,11 @@ def build_store_fp4(K: torch.Tensor, V: torch.Tensor, out: StoreFp4 | None = Non
 def attend_fp4(Q: torch.Tensor, store: StoreFp4, q_chunk: int = 16384, kv_block: int = 0,
                softmax_scale: float = 0.0, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """h3kv_attend_fp4: kvfp4 attention of bf16 Q [heads, q_seq, 128] -> fp32."""
+    _need_rows(Q, "Q", store.heads)
     q_seq = int(Q.shape[1])
     with _on(stream):
         out = torch.empty(Q.shape, dtype=torch.float32, device=Q.device) if out is None else out
+    _need_out(out, Q)
     st = store.c_struct()
     check(h3kv_attend_fp4(_ptr(Q), q_seq, ctypes.byref(st), int(q_chunk), int(kv_block), float(softmax_scale),
                           _ptr(out), _stream(stream)), "h3kv_attend_fp4")
