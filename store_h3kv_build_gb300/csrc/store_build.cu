@@ -42,10 +42,35 @@ struct RowScale {
   bool clamp;
   float m;
 };
+
+// x / 127 rounded to nearest: x * RN(1/127) corrected once by its exact
+// residual (Markstein's division step).  Checked on the host against IEEE
+// division for every non-negative finite fp32 x; infinities and NaN take
+// x * RN(1/127), which is what division gives them.  About a third of the
+// instructions of the library's correctly rounded division.
+__device__ __forceinline__ float div127(float x) {
+  constexpr float kRcp127 = 0.007874015718698502f;  // RN(1/127), 0x3C010204
+  const float q0 = __fmul_rn(x, kRcp127);
+  if (!(x < INFINITY)) return q0;
+  const float r = __fmaf_rn(-q0, 127.0f, x);
+  return __fmaf_rn(r, kRcp127, q0);
+}
+
+// 1 / p rounded to nearest for p = RN(s * sqrt(128)), s a positive finite
+// fp16 scale: the hardware's approximate reciprocal refined by one fma step.
+// Checked on the host for every such p and every starting value within two
+// ulp of 1 / p.
+__device__ __forceinline__ float rcp_scale(float p) {
+  float y0;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y0) : "f"(p));
+  const float e = __fmaf_rn(-p, y0, 1.0f);
+  return __fmaf_rn(e, y0, y0);
+}
+
 __device__ __forceinline__ RowScale row_scale(float amax) {
   RowScale rs;
   const float a = amax * kInvSqrt128;
-  rs.sh = __float2half_rn(__fdiv_rn(a, 127.0f));
+  rs.sh = __float2half_rn(div127(a));
   rs.clamp = false;
   if (__hisinf(rs.sh)) {
     rs.sh = __ushort_as_half(0x7BFFu);  // 65504
@@ -53,7 +78,7 @@ __device__ __forceinline__ RowScale row_scale(float amax) {
   }
   const float sf = __half2float(rs.sh);
   rs.clamp = rs.clamp || (sf < 6.103515625e-05f);  // fp16 subnormal scale: x'/s may exceed 127.5
-  rs.m = sf > 0.f ? __frcp_rn(sf * 11.313708498984761f) : 0.f;
+  rs.m = sf > 0.f ? rcp_scale(sf * 11.313708498984761f) : 0.f;
   return rs;
 }
 
