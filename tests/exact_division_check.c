@@ -1,9 +1,12 @@
-// Exhaustive host checks of the store build's scale arithmetic (store_build.cu,
-// div127 and rcp_scale), in IEEE fp32 with a fused fma:
+// Exhaustive host checks of the kvi8r store build's scale arithmetic
+// (store_build.cu: div127, rcp_scale), in IEEE fp32 with a fused fma:
 //  (1) q1 = fma(fma(-q0, 127, a), y, q0), q0 = a * y, y = RN(1/127), equals a / 127 (RN) for every
 //      non-negative finite fp32 a;
 //  (2) y1 = fma(fma(-p, y0, 1), y0, y0) equals 1 / p (RN) for every p = RN(sf * c), sf a positive finite
 //      fp16 value, c = 11.313708498984761f, and every y0 within 2 ulp of 1 / p.
+// (The same quotient step with 448 fails where the quotient is subnormal, and the same reciprocal step
+// for an arbitrary s fails from starts 2 ulp away on some significands: the kvf8s build keeps the
+// library's division and reciprocal.)
 #include <math.h>
 #include <stdint.h>
 #include <stdio.h>
