@@ -29,16 +29,21 @@ Readings where the pages leave a step open:
       channel); the store encodes k' - mu.  Subtracting mu shifts every score
       of a query row by the same q'.mu, so the softmax is unchanged; mu is
       kept only as a diagnostic.
-  R16 K scale: one fp32 scale per (head, 64-token block) s = absmax/448 over
-      the block's smoothed values (a tail block covers the tokens it has);
-      codes = e4m3(x r) with r = fp32(1/s), the scale's reciprocal rounded to
-      fp32 (the encode multiplies by it); a block with s = 0 has all codes 0.
+  R16 K scale: one fp32 scale per (head, 64-token block) s = absmax/448
+      over the block's smoothed values (a tail block covers the tokens it
+      has); codes = e4m3(x / s), the quotient rounded once, exactly, to the
+      nearest e4m3 value (ties to even); a block with s = 0 has all codes 0.
   R17 V scale: one fp32 scale per (head, channel) s = absmax/448 over all
-      tokens; codes = e4m3(v r), r = fp32(1/s), with the product taken in fp32
-      (v is bf16, so both sides decide every V code in the same precision).
+      tokens; codes = e4m3(v / s) rounded once from the exact quotient, as
+      for K.
   R18 Q: one fp32 scale per rotated query row, s = absmax/448, codes =
-      e4m3(q' r), r = fp32(1/s); the scores are
+      e4m3(q' / s) rounded from the exact quotient; the scores are
       S = (code_q . code_k) s_q s_k * scale.
+      Reading for R16-R18: the pages name "fp8 e4m3 V per channel" and "fp8
+      K/V if a kernel takes it without dequant" and give no arithmetic; the
+      plainest reading of a scaled encode is the value divided by its scale,
+      rounded once.  How a kernel forms the quotient (a reciprocal and a
+      product, say) is its own precision step, bounded in its tests.
   R19 The result is exact softmax attention over the dequantised encodings
       (reading R7's blockwise combine changes nothing mathematically).  The
       fp8 P of a kernel's P.V product is a precision step of that kernel,
@@ -101,18 +106,38 @@ def fp32_round(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
 
 
-def fp32_recip(s) -> np.ndarray:
-    """fp32(1/s) of fp32 scales (1 where s = 0, never used there)."""
-    s32 = np.asarray(s, dtype=np.float64).astype(np.float32)
-    with np.errstate(divide="ignore"):
-        return np.where(s32 > 0, np.float32(1) / np.where(s32 > 0, s32, np.float32(1)), np.float32(1))
+def e4m3_div(x, s) -> np.ndarray:
+    """Codes (uint8) of x / s rounded once to the nearest e4m3 value, ties to
+    the even code, saturating at +-448; the sign follows x (readings
+    R16-R18).  x is fp64 and s a positive fp32 value (broadcast against x).
+
+    The quotient is never rounded to fp64 first.  The two e4m3 values that
+    bracket |x| / s are found from the fp64 quotient; the choice between them
+    compares |x| with their midpoint times s.  A midpoint of two e4m3 values
+    has at most 5 significant bits and s 24, so that product is exact in
+    fp64, and the sign of the fp64 difference |x| - m s is the sign of the
+    exact one."""
+    x = np.asarray(x, dtype=np.float64)
+    s = np.broadcast_to(np.asarray(s, dtype=np.float64), x.shape)
+    a = np.abs(x)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = a / s
+    lo = np.searchsorted(_POS, q, side="right") - 1    # _POS[lo] <= fp64 quotient
+    lo = np.clip(lo, 0, len(_POS) - 1)
+    hi = np.minimum(lo + 1, len(_POS) - 1)
+    mid = (_POS[lo] + _POS[hi]) / 2                    # exact: 5 significant bits at most
+    d = a - mid * s                                    # sign of |x| - mid s, exact
+    pick_hi = (d > 0) | ((d == 0) & (hi % 2 == 0))
+    mag = np.where(lo == hi, lo, np.where(pick_hi, hi, lo)).astype(np.uint8)  # lo == hi: 448, saturated
+    return np.where(np.signbit(x), mag | np.uint8(0x80), mag).astype(np.uint8)
 
 
 def _scaled_codes(x: np.ndarray, s: np.ndarray) -> np.ndarray:
-    """e4m3(x * fp32(1/s)) with s broadcast against x; all-zero codes where
-    s = 0 (readings R16, R18)."""
-    r = fp32_recip(s).astype(np.float64)
-    return np.where(s > 0, e4m3_encode(x * r), np.uint8(0)).astype(np.uint8)
+    """e4m3(x / s) with s broadcast against x; all-zero codes where s = 0
+    (readings R16-R18)."""
+    s = np.broadcast_to(np.asarray(s, dtype=np.float64), np.shape(x))
+    pos = s > 0
+    return np.where(pos, e4m3_div(x, np.where(pos, s, 1.0)), np.uint8(0)).astype(np.uint8)
 
 
 # --------------------------------------------------------------------------
@@ -152,13 +177,9 @@ def v_channel_scales(V) -> np.ndarray:
 
 def encode_v(V) -> dict:
     """V codes [heads, seq, 128] (token-major here) and fp32 per-channel
-    scales [heads, 128]; each product v * fp32(1/s) in fp32 (R17)."""
-    v32 = as_f64(V).astype(np.float32)
+    scales [heads, 128]; codes e4m3(v / s) (R17)."""
     s = v_channel_scales(V)
-    r = fp32_recip(s)[:, None, :]
-    q = (v32 * r).astype(np.float64)
-    codes = np.where(s[:, None, :] > 0, e4m3_encode(q), np.uint8(0)).astype(np.uint8)
-    return {"v_codes": codes, "v_scales": s}
+    return {"v_codes": _scaled_codes(as_f64(V), s[:, None, :]), "v_scales": s}
 
 
 def build_store_kvf8s(K, V, block: int = K_BLOCK) -> dict:
@@ -204,7 +225,7 @@ def attend_kvf8s(Q, store: dict, scale: float | None = None, heads=None, block: 
 
 
 __all__ = [
-    "E4M3_MAX", "K_BLOCK", "HEAD_DIM", "e4m3_values", "e4m3_encode", "e4m3_decode", "fp32_round", "fp32_recip",
+    "E4M3_MAX", "K_BLOCK", "HEAD_DIM", "e4m3_values", "e4m3_encode", "e4m3_decode", "e4m3_div", "fp32_round",
     "smooth_mean", "k_block_scales", "encode_k", "v_channel_scales", "encode_v", "build_store_kvf8s",
     "dequant_k", "dequant_v", "encode_q", "attend_kvf8s",
 ]

@@ -1,9 +1,13 @@
 """Pins of the kvf8s oracle (fp8 e4m3 store in the kvi8s layout) against what
 the pages and the mathematics fix, independent of the oracle's own code:
-the e4m3 format's defining values, PyTorch's float8_e4m3fn cast, closed-form
-special cases of attention, the softmax invariance that mean smoothing rests
-on, and error bounds of round-to-nearest.
+the e4m3 format's defining values, PyTorch's float8_e4m3fn cast, the scaled
+encode e4m3(x / s) against exact rational rounding and hand-worked ties,
+closed-form special cases of attention (one of them analytic in the query's
+scale), the softmax invariance that mean smoothing rests on, and error
+bounds of round-to-nearest.
 """
+from fractions import Fraction
+
 import numpy as np
 import pytest
 import torch
@@ -110,21 +114,135 @@ def test_k_dequant_error_bound():
     assert np.all(err <= bound)
 
 
-def test_v_channel_scale_and_codes():
-    # R17: per channel the largest |v| encodes to +-448; the codes are the
-    # fp32 product v * fp32(1/s) rounded to e4m3, which PyTorch's fp32
-    # arithmetic and e4m3 cast reproduce
+def _e4m3_brute(x: Fraction) -> int:
+    """The e4m3 code nearest to the exact rational x, ties to the even code,
+    saturating at 448: a search over the format's values, from the bit
+    fields, in exact rational arithmetic."""
+    vals = []
+    for c in range(0x7F):
+        e, m = c >> 3, c & 7
+        v = Fraction(m, 8) * Fraction(1, 64) if e == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+        vals.append((v, c))
+    a = min(abs(x), Fraction(448))
+    best = min(vals, key=lambda vc: (abs(vc[0] - a), vc[1] & 1))
+    return best[1] | (0x80 if x < 0 else 0)
+
+
+def test_e4m3_div_matches_exact_rational_rounding():
+    # brute force: the quotient of a bf16 or fp64 value by an fp32 scale,
+    # rounded in exact rational arithmetic (no floating point anywhere)
+    rng = np.random.default_rng(12)
+    x = np.concatenate([
+        rng.standard_normal(1500) * np.exp2(rng.integers(-10, 6, 1500)),
+        synth.normal_f32((1, 1, 1500), 4).to(torch.bfloat16).double().numpy().ravel(),
+    ])
+    s = f8.fp32_round(np.abs(rng.standard_normal(x.size)) * np.exp2(rng.integers(-8, 2, x.size)) + 1e-3)
+    got = f8.e4m3_div(x, s)
+    ref = np.array([_e4m3_brute(Fraction(float(a)) / Fraction(float(b))) for a, b in zip(x, s)])
+    assert np.array_equal(got, ref)
+
+
+def test_e4m3_div_ties_that_a_reciprocal_product_misses():
+    # scale 12.25 / 448 = 7/256, exact in fp32.  0.1708984375 / (7/256) = 6.25
+    # exactly, the midpoint of 6 (0x4c) and 6.5 (0x4d): the tie goes to the
+    # even code 0x4c.  The fp32 reciprocal 256/7 rounds up, so the fp32
+    # product v * fp32(1/s) lands just above 6.25 and would give 0x4d.
+    # Likewise 0.000347137451171875 / s = 6.5 * 2^-9, halfway between the
+    # subnormals 6 * 2^-9 (0x06) and 7 * 2^-9 (0x07): 0x06.
+    s = 7.0 / 256.0
+    x = np.array([0.1708984375, 0.000347137451171875, -0.1708984375, 12.25, 1.0, 0.5, s, s / 2, 0.0])
+    # hand-worked: 6.25 -> 0x4c; 6.5 * 2^-9 -> 0x06; sign bit; 448 -> 0x7e;
+    # 36.57.. -> 36 (0x61); 18.29.. -> 18 (0x59); 1.0 -> 0x38; 0.5 -> 0x30; 0
+    assert list(f8.e4m3_div(x, s)) == [0x4C, 0x06, 0xCC, 0x7E, 0x61, 0x59, 0x38, 0x30, 0x00]
+    r = np.float32(1) / np.float32(s)
+    assert f8.e4m3_encode(np.float64(np.float32(0.1708984375) * r)) == 0x4D  # the product's answer
+
+
+def test_e4m3_div_by_powers_of_two_is_the_cast():
+    # a power-of-two scale divides exactly, so the code is the (torch-pinned)
+    # rounding of x * 2^-k itself
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal(20000) * np.exp2(rng.integers(-12, 8, 20000))
+    for k in (-6, 0, 3):
+        assert np.array_equal(f8.e4m3_div(x, 2.0 ** k), f8.e4m3_encode(x / 2.0 ** k))
+
+
+def test_v_channel_codes_hand_worked():
+    # R17 on a channel whose absmax is 12.25: s_v = 12.25 / 448 = 7/256, and
+    # the codes are the hand-worked quotients above; a second channel of
+    # constant 3.5 has s_v = 1/128 and every code 448 (0x7e); a zero channel
+    # has s_v = 0 and zero codes
+    col = [12.25, 0.1708984375, 0.000347137451171875, -0.1708984375, 1.0, 0.5, 7.0 / 256.0, 7.0 / 512.0, 0.0]
+    v = torch.zeros((1, len(col), 128), dtype=torch.float64)
+    v[0, :, 0] = torch.tensor(col, dtype=torch.float64)
+    v[0, :, 1] = 3.5
+    st = f8.encode_v(v.to(torch.bfloat16))
+    assert st["v_scales"][0, 0] == 7.0 / 256.0 and st["v_scales"][0, 1] == 1.0 / 128.0
+    assert st["v_scales"][0, 2] == 0.0
+    assert list(st["v_codes"][0, :, 0]) == [0x7E, 0x4C, 0x06, 0xCC, 0x61, 0x59, 0x38, 0x30, 0x00]
+    assert np.all(st["v_codes"][0, :, 1] == 0x7E) and not st["v_codes"][0, :, 2:].any()
+
+
+def test_v_scale_maps_channel_absmax_to_448():
+    # per channel the largest |v| encodes to +-448 and no code is NaN
     _, _, v = synth.make_qkv(2, 100, seed=6)
     st = f8.encode_v(v)
     vv = v.float()
-    s = vv.abs().amax(dim=1) / 448.0
-    assert np.array_equal(st["v_scales"], s.double().numpy())
-    ref = (vv * (1.0 / s)[:, None, :]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
-    assert np.array_equal(st["v_codes"], ref)
+    assert np.array_equal(st["v_scales"], (vv.abs().amax(dim=1) / 448.0).double().numpy())
+    assert np.all((st["v_codes"] & 0x7F) != 0x7F)
     idx = vv.abs().argmax(dim=1)
     for h in range(2):
         for d in range(0, 128, 17):
             assert st["v_codes"][h, idx[h, d], d] & 0x7F == 0x7E
+
+
+def _rotated_one_hot(coeffs: dict) -> torch.Tensor:
+    """A bf16 row q with q H = sqrt(128) * sum_c coeffs[c] e_c: row c of
+    sqrt(128) H is a +-1 pattern, so q's entries are sums of +-coeffs."""
+    Hs = np.sign(oracle.hadamard())  # +-1 Sylvester matrix
+    q = sum(a * Hs[c] for c, a in coeffs.items())
+    out = torch.tensor(q, dtype=torch.float64).to(torch.bfloat16)
+    assert torch.equal(out.double(), torch.tensor(q))
+    return out
+
+
+def test_encode_q_codes_of_a_rotated_one_hot_row():
+    # q' = sqrt(128) (0.25 e_5 + 0.125 e_40): s_q = fp32(0.25 sqrt(128) / 448),
+    # the channel-5 value encodes to 448 (0x7e), channel 40 to 224 (0x76),
+    # every other channel to (+-)0 -- codes that do not depend on s_q's
+    # rounding (the fp64 rotation leaves values near 1e-17 off the two
+    # channels, whose sign the zero code keeps)
+    q = _rotated_one_hot({5: 0.25, 40: 0.125})[None, None, :]
+    codes, s = f8.encode_q(q)
+    assert codes[0, 0, 5] == 0x7E and codes[0, 0, 40] == 0x76
+    assert not (np.delete(codes[0, 0], [5, 40]) & 0x7F).any()
+    assert abs(s[0, 0] * 448.0 / (0.25 * np.sqrt(128.0)) - 1.0) < 2.0 ** -23
+
+
+def test_attend_two_keys_closed_form_uses_the_query_scale():
+    # query q' = a e_5, keys k1' = b e_5 and k2' = -b e_5 (a = b =
+    # 0.25 sqrt(128); their mean is 0, so smoothing changes nothing), values
+    # v1 = (7, 3.5, 0..), v2 = (-7, 3.5, 0..).  Every code is +-448 or 0, and
+    # 7 / 448, 3.5 / 448 are powers of two, so dequantised V is exact.  With
+    # scores +-a b * scale the softmax gives channel 0 = 7 tanh(a b scale) and
+    # channel 1 = 3.5; a and b enter only through 448 * s_q and 448 * s_k,
+    # each within 2^-24 of the exact value.  Dropping s_q (or a missing
+    # rotation of q) moves channel 0 far from the closed form.
+    a = b = 0.25 * np.sqrt(128.0)
+    q = _rotated_one_hot({5: 0.25})[None, None, :]
+    k1 = _rotated_one_hot({5: 0.25})
+    k = torch.stack([k1, -k1])[None]
+    v = torch.zeros((1, 2, 128), dtype=torch.float64)
+    v[0, 0, :2] = torch.tensor([7.0, 3.5])
+    v[0, 1, :2] = torch.tensor([-7.0, 3.5])
+    st = f8.build_store_kvf8s(k, v.to(torch.bfloat16))
+    scale = 1.0 / np.sqrt(128.0)
+    out = f8.attend_kvf8s(q, st, scale=scale)[0, 0]
+    assert abs(out[0] - 7.0 * np.tanh(a * b * scale)) < 7.0 * 4e-7
+    assert abs(out[1] - 3.5) < 1e-12 and not out[2:].any()
+    # a sharper softmax scale moves the closed form the same way
+    out2 = f8.attend_kvf8s(q, st, scale=4 * scale)[0, 0]
+    assert abs(out2[0] - 7.0 * np.tanh(4 * a * b * scale)) < 7.0 * 4e-7
 
 
 def test_zero_inputs_have_zero_codes():
