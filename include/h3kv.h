@@ -144,10 +144,14 @@ size_t h3kv_staging_bytes(int32_t heads, int32_t kv_block);
  * `state` (device fp32 [store->heads, q_seq, 2]: running max and sum per
  * query row) with O itself as the running un-normalised output.  The result
  * is bit-identical to h3kv_attend on the same store, q_chunk and kv_block.
- * Arguments otherwise as h3kv_attend; `store` may point to host (pinned for
- * asynchronous copies) or device memory, and must have per-row scales
- * (scale_group 0 or 128; H3KV_ERR_UNSUPPORTED otherwise).  The library
- * allocates nothing:
+ * Arguments otherwise as h3kv_attend; `store` may point to device, managed
+ * or pinned (page-locked) host memory, and must have per-row scales
+ * (scale_group 0 or 128; H3KV_ERR_UNSUPPORTED otherwise).  A store buffer in
+ * pageable host memory is refused (H3KV_ERR_INVALID_ARG) before any work:
+ * copies from pageable memory take its bytes when they are issued, not in
+ * stream order, so a store built into it by earlier work still queued on
+ * the GPU would be read before it is written.  The library allocates
+ * nothing:
  * staging and state are caller-owned scratch, reused by each call, so calls
  * that overlap on the GPU must not share them.
  * With staging_bytes >= round_up(h3kv_staging_bytes(...), 256) +
@@ -229,9 +233,11 @@ h3kv_status h3kv_attend_staged_static(const uint16_t *Q, int64_t q_seq, const h3
  *      row by the same amount, so attention does not need it; it is stored
  *      for inspection.
  *   V: not rotated; per (head, channel) s_v = max over all tokens |v| / 448;
- *      codes e4m3(v / s_v) (fp32 quotient), stored channel-major (V
- *      transposed) with a row stride of h3kv_f8_v_stride(seq) bytes; bytes
- *      of a row past seq are 0.
+ *      codes e4m3(v / s_v), the exact quotient rounded once (bit-exact),
+ *      stored channel-major (V transposed) with a row stride of
+ *      h3kv_f8_v_stride(seq) bytes; bytes of a row past seq are 0.
+ *   The K (and query) codes are the same rounding of quotients of values
+ *   that the kernels compute in fp32, formed as x * fp32(1/s).
  * Every buffer is caller-owned device memory, 16-byte aligned. */
 typedef struct {
   uint8_t *k_codes;   /* e4m3 [heads, seq, 128] */

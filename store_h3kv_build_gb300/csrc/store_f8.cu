@@ -5,10 +5,11 @@
 //
 //   K: k' = k H (the 128-wide Hadamard basis), smoothed by mu = the mean of
 //      k' over all tokens of the head, one fp32 scale per 64-token block
-//      s = absmax / 448, codes e4m3(x * fp32(1/s)).
+//      s = absmax / 448, codes e4m3(x / s), formed as x * fp32(1/s).
 //   V: not rotated; one fp32 scale per (head, channel) s = absmax over all
-//      tokens / 448, codes e4m3(v * fp32(1/s)), stored channel-major [heads,
-//      128, v_stride] (V transposed) so that P.V reads it K-major.
+//      tokens / 448, codes e4m3(v / s) with the quotient rounded once,
+//      exactly (e4m3_quotient below), stored channel-major [heads, 128,
+//      v_stride] (V transposed) so that P.V reads it K-major.
 //
 // Two passes: a statistics pass (the K mean and the V channel absmax of
 // every head) and an encode pass.  Both are HBM streams; every sum is taken
@@ -187,6 +188,38 @@ __device__ __forceinline__ void transpose4x4(uint32_t a, uint32_t b, uint32_t e,
   out[3] = __byte_perm(t1, t3, 0x7632);
 }
 
+// The fp32 value whose e4m3 rounding (cvt.rn.satfinite) is the code of the
+// quotient v / s rounded once, exactly, to the nearest e4m3 value (ties to
+// the even code), given r16 = fp32(1/s) * 2^16 and t = fp32(v * fp32(1/s)).
+// t lies within two fp32 ulps of the quotient, so the two round differently
+// only when an e4m3 rounding boundary -- the midpoint m of two neighbouring
+// e4m3 values -- lies that close to t.  bf16 values over an fp32 scale land
+// there often (about 1e-3 of N(0, 1) codes), so every such case is decided
+// by the sign of |v| - m s: m has at most five significant bits and s 24, so
+// the fma's single rounding keeps the sign of the exact difference.
+//  - |t| >= 2^-6 (e4m3 normal range): the boundary inside t's cell is |t|
+//    with its 20 low mantissa bits set to 0x80000.
+//  - |t| < 2^-6 (e4m3 subnormals, spacing 2^-9): u = |t| + 2^-6 lies in the
+//    binade [2^-6, 2^-5), whose e4m3 cells are 2^-9 wide as well, so the
+//    same bits of u give the boundary m + 2^-6.
+// Near a boundary the returned magnitude m + (|v| - m s) r16 sits on the
+// quotient's side of m, at least one fp32 ulp and at most a quarter of the
+// e4m3 spacing away -- or is m itself on an exact tie, which the conversion
+// rounds to the even code.  No branch: every element takes the same steps.
+// The procedure was checked against exact rational rounding of the quotient
+// on 5e7 bf16 values before it ran on a GPU.
+__device__ __forceinline__ float e4m3_quotient(float v, float s, float r16, float t) {
+  const float at = fabsf(t);
+  const bool sub = at < 0x1p-6f;
+  const float u = sub ? at + 0x1p-6f : at;
+  const uint32_t ub = __float_as_uint(u);
+  const float mu = __uint_as_float((ub & 0xFFF00000u) | 0x00080000u);
+  const float m = sub ? mu - 0x1p-6f : mu;
+  const float tn = fmaf(fmaf(-m, s, fabsf(v)), r16, m);
+  const bool near = ((ub & 0xFFFFFu) - 0x7FFFDu) < 7u;
+  return copysignf(near ? tn : at, v);
+}
+
 constexpr int kEncRows = 128;                  // tokens per tile = compute threads
 constexpr int kEncStages = 3;                  // input ring depth (2 CTAs per SM)
 constexpr int kEncTileBytes = kEncRows * 256;  // bf16 [128 tokens x 128 channels]
@@ -196,6 +229,8 @@ struct EncSmem {
   uint8_t in[kEncStages][kEncTileBytes];  // 1024-byte aligned (128-byte swizzle)
   float neg_mu[128];   // -mean(k') of the current head
   float rv[128];       // fp32(1 / s_v) per V channel, 0 where s_v = 0
+  float sv[128];       // s_v per V channel
+  float rv16[128];     // fp32(1 / s_v) * 2^16
   uint32_t keep[32];   // byte mask of the V channels with s_v > 0
   float warp_amax[4];  // K: per-warp absmax (warps 0-1: first 64 tokens of the tile)
   uint64_t full[kEncStages];
@@ -224,7 +259,7 @@ __device__ __forceinline__ uint32_t vstage_off(uint32_t r, uint32_t g) {
 //     k' = fp32(x / sqrt 128) - mu rounded to fp32, the absmax of each
 //     64-token block by a warp reduction and one 128-thread barrier, then
 //     the row's codes straight to global memory.
-//   V tile: the row's codes e4m3(v * fp32(1/s_v)) are written back into the
+//   V tile: the row's codes e4m3(v / s_v) are written back into the
 //     drained stage, then each thread reads four channels of 32 tokens,
 //     transposes them in registers and stores 32-token pieces of four
 //     channel rows of the transposed V.
@@ -306,6 +341,8 @@ __global__ void __launch_bounds__(kEncThreads, 2)
         named_bar_sync(1, kEncRows);
         sm.neg_mu[r] = -mu;
         sm.rv[r] = sv > 0.f ? __frcp_rn(sv) : 0.f;
+        sm.sv[r] = sv;
+        sm.rv16[r] = sm.rv[r] * 65536.f;
         reinterpret_cast<uint8_t *>(sm.keep)[r] = sv > 0.f ? 0xFFu : 0u;
         named_bar_sync(1, kEncRows);
         cur_h = h;
@@ -397,13 +434,20 @@ __global__ void __launch_bounds__(kEncThreads, 2)
                 *reinterpret_cast<const uint4 *>(tile + (gi >> 3) * (kEncTileBytes / 2) + sw128_off(r, gi & 7));
             const float4 r0 = *reinterpret_cast<const float4 *>(&sm.rv[8 * gi]);
             const float4 r1 = *reinterpret_cast<const float4 *>(&sm.rv[8 * gi + 4]);
-            float v[8];
+            const float4 s0 = *reinterpret_cast<const float4 *>(&sm.sv[8 * gi]);
+            const float4 s1 = *reinterpret_cast<const float4 *>(&sm.sv[8 * gi + 4]);
+            const float4 q0 = *reinterpret_cast<const float4 *>(&sm.rv16[8 * gi]);
+            const float4 q1 = *reinterpret_cast<const float4 *>(&sm.rv16[8 * gi + 4]);
+            const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+            const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+            const float r16[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+            float v[8], t[8];
             bf16x4(make_uint2(in.x, in.y), *reinterpret_cast<float(*)[4]>(v));
             bf16x4(make_uint2(in.z, in.w), *reinterpret_cast<float(*)[4]>(v + 4));
-            w[2 * gi] = pack_e4m3x4(__fmul_rn(v[0], r0.x), __fmul_rn(v[1], r0.y), __fmul_rn(v[2], r0.z),
-                                    __fmul_rn(v[3], r0.w));
-            w[2 * gi + 1] = pack_e4m3x4(__fmul_rn(v[4], r1.x), __fmul_rn(v[5], r1.y), __fmul_rn(v[6], r1.z),
-                                        __fmul_rn(v[7], r1.w));
+#pragma unroll
+            for (int k = 0; k < 8; ++k) t[k] = e4m3_quotient(v[k], ss[k], r16[k], __fmul_rn(v[k], rr[k]));
+            w[2 * gi] = pack_e4m3x4(t[0], t[1], t[2], t[3]);
+            w[2 * gi + 1] = pack_e4m3x4(t[4], t[5], t[6], t[7]);
           }
         }
 #pragma unroll

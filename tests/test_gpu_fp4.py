@@ -14,9 +14,11 @@ Bars:
     step apart; K codes in the blocks whose scales agree: identical except at
     most 1e-3 of them, each on a neighbouring e2m1 value (the GPU rotates in
     fp32, the oracle in fp64);
-  * attention: against the oracle's attention over the GPU-built store, the
-    kvi8r bar (max abs 2e-2, mean abs 2e-3): the store's values are exact in
-    fp16, so only the fp16 query and fp16 softmax weights round.
+  * attention: the kvi8r bar (max abs 2e-2, mean abs 2e-3), both against the
+    oracle's attention over the GPU-built store (the store's values are exact
+    in fp16, so only the fp16 query and fp16 softmax weights round) and end
+    to end against the oracle's attention over its own store (tiny, 24 x
+    32768 on four heads, 32 x 217088 on eight heads).
 """
 import numpy as np
 import pytest
@@ -85,6 +87,12 @@ def compare_fp4_attention(out, Q, store, what="", scale=None):
     """GPU output vs the oracle's attention over the same (GPU-built) store."""
     ref = f4.attend_kvfp4(Q, store, scale=scale)
     return compare_attention(out, ref, what)
+
+
+def oracle_store_heads(K, V, heads):
+    """The oracle's own kvfp4 store of the listed heads (stacked in order)."""
+    parts = [f4.build_store_kvfp4(K[h:h + 1], V[h:h + 1]) for h in heads]
+    return {k: np.concatenate([p[k] for p in parts]) for k in parts[0]}
 
 
 # ------------------------------------------------------------------ store --
@@ -193,6 +201,33 @@ def test_attend_fp4_against_oracle_store(cuda):
     compare_fp4_attention(out, q, f4.build_store_kvfp4(k, v), "against the oracle store")
 
 
+def test_attend_fp4_end_to_end_tiny(cuda):
+    b = _b()
+    q, k, v = synth.make_qkv(1, 1024, seed=0)
+    st = _build(k.to(cuda), v.to(cuda))
+    out = b.attend_fp4(q.to(cuda), st, q_chunk=256, kv_block=512)
+    b.sync_status()
+    mx, mean = compare_fp4_attention(out, q, f4.build_store_kvfp4(k, v), "tiny, oracle store")
+    print(f"kvfp4 end to end tiny: max abs {mx:.3e} mean abs {mean:.3e}")
+
+
+def test_attend_fp4_end_to_end_h24_l32768_outlier(cuda):
+    # end to end on the outlier workload in its launch configuration: four
+    # heads, 256 sampled query rows each, against the oracle's store of those
+    # heads over all 32768 keys
+    b = _b()
+    w = synth.WORKLOADS["h24_l32768_outlier"]
+    q, k, v = synth.make_qkv(w["heads"], w["seq"], seed=0, k_outliers=True)
+    st = _build(k.to(cuda), v.to(cuda))
+    out = b.attend_fp4(q.to(cuda), st, q_chunk=w["q_chunk"], kv_block=w["kv_block"])
+    b.sync_status()
+    heads = [0, 7, 13, 23]
+    rows = torch.randperm(w["seq"], generator=torch.Generator().manual_seed(2))[:256].sort().values
+    mx, mean = compare_fp4_attention(out[heads][:, rows.to(cuda)], q[heads][:, rows],
+                                     oracle_store_heads(k, v, heads), "h24 l32768 outlier, oracle store")
+    print(f"kvfp4 end to end h24 l32768: max abs {mx:.3e} mean abs {mean:.3e}")
+
+
 def test_attend_fp4_q_chunk_invariance(cuda):
     b = _b()
     q, k, v = synth.make_qkv(2, 3000, seed=3, k_outliers=True, device=cuda)
@@ -245,7 +280,8 @@ def test_attend_fp4_h24_l32768_sampled(cuda):
 @pytest.mark.slow
 def test_fp4_full_size_h32_l217088(cuda):
     # the full-size workload in the launch configuration the bench times:
-    # store heads 0 and 31 in full; attention on 64 sampled rows x 8 heads
+    # store heads 0 and 31 in full; attention on 64 sampled rows x 8 heads,
+    # over the GPU store and end to end over the oracle's own store
     b = _b()
     w = synth.WORKLOADS["h32_l217088_outlier"]
     q, k, v = synth.make_qkv(w["heads"], w["seq"], seed=0, k_outliers=True, device=cuda)
@@ -257,8 +293,12 @@ def test_fp4_full_size_h32_l217088(cuda):
     b.sync_status()
     heads = [0, 5, 9, 13, 17, 21, 26, 31]
     rows = torch.linspace(0, w["seq"] - 1, 64).long()
-    compare_fp4_attention(out[heads][:, rows], q[heads][:, rows].cpu(), gpu_store_numpy(st, heads),
-                          "h32 l217088 sampled")
+    qs = q[heads][:, rows].cpu()
+    compare_fp4_attention(out[heads][:, rows], qs, gpu_store_numpy(st, heads), "h32 l217088 sampled")
+    # end to end against the oracle's own store of the eight heads
+    mx, mean = compare_fp4_attention(out[heads][:, rows], qs, oracle_store_heads(kc, vc, heads),
+                                     "h32 l217088, oracle store")
+    print(f"kvfp4 end to end h32 l217088: max abs {mx:.3e} mean abs {mean:.3e}")
 
 
 def test_attend_fp4_calls_on_one_output_stay_in_stream_order(cuda):
