@@ -22,6 +22,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 HEAD_DIM = 128
 DEFAULT_KV_BLOCK = 16384
 KV_TILE = 128
+H3KV_STATIC_SCRATCH_BYTES = 32 * 1024 * 1024  # the fixed scratch of h3kv_attend_staged_static
 
 H3KV_OK = 0
 H3KV_ERR_INVALID_ARG = 1
@@ -180,11 +181,12 @@ class Store:
             kw = dict(pin_memory=True)
         else:
             kw = dict(device=device)
-        kc = torch.empty((heads, seq, HEAD_DIM), dtype=torch.int8, **kw)
-        vc = torch.empty_like(kc)
+        # every buffer allocated with its own pin_memory request: empty_like
+        # of a pinned tensor is pageable, and h3kv_attend_staged refuses a
+        # store with pageable buffers
         sshape = (heads, seq, HEAD_DIM // 32) if scale_group == 32 else (heads, seq)
-        ks = torch.empty(sshape, dtype=torch.float16, **kw)
-        vs = torch.empty_like(ks)
+        kc, vc = (torch.empty((heads, seq, HEAD_DIM), dtype=torch.int8, **kw) for _ in range(2))
+        ks, vs = (torch.empty(sshape, dtype=torch.float16, **kw) for _ in range(2))
         return cls(kc, vc, ks, vs)
 
     @property

@@ -147,6 +147,18 @@ int scale_groups_of(const h3kv_store *st) {
   return 0;
 }
 
+// Whether copies from `p` run in stream order: device, managed or pinned
+// host memory.  Pageable host memory is not (its copies read it when they
+// are issued).
+bool copy_engine_ordered(const void *p) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the error the query may leave
+    return false;
+  }
+  return attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged || attr.type == cudaMemoryTypeHost;
+}
+
 float scale_log2_of(float softmax_scale) {
   const float s = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(128.0f);
   return s * 1.4426950408889634f;
@@ -316,6 +328,12 @@ h3kv_status h3kv_attend_staged(const uint16_t *Q, int64_t q_seq, const h3kv_stor
   if (!aligned16(Q) || !aligned16(O) || !aligned16(staging) || !aligned16(state)) return H3KV_ERR_INVALID_ARG;
   const int64_t kvb = kv_block == 0 ? H3KV_DEFAULT_KV_BLOCK : kv_block;
   if (staging_bytes < h3kv_staging_bytes(store->heads, static_cast<int32_t>(kvb))) return H3KV_ERR_INVALID_ARG;
+  // the block copies are stream-ordered only from device, managed or pinned
+  // memory: from pageable memory the driver takes the bytes when the copy is
+  // issued, before earlier work in the stream (a store build, say) has run
+  for (const void *p : {static_cast<const void *>(store->k_codes), static_cast<const void *>(store->v_codes),
+                        static_cast<const void *>(store->k_scales), static_cast<const void *>(store->v_scales)})
+    if (!copy_engine_ordered(p)) return H3KV_ERR_INVALID_ARG;
   DeviceInfo *d = nullptr;
   st = device_info(&d);
   if (st != H3KV_OK) return st;

@@ -40,15 +40,23 @@ h3kv_status scratch_address(void **out) {
 extern "C" h3kv_status h3kv_attend_staged_static(const uint16_t *Q, int64_t q_seq, const h3kv_store *store,
                                                  int32_t q_chunk, int32_t kv_block, float softmax_scale, float *O,
                                                  void *stream) {
-  if (!store || q_seq < 0 || store->heads < 0) return H3KV_ERR_INVALID_ARG;
+  // the argument checks h3kv_attend_staged makes first, in its order, so that
+  // a store it does not take gets the same status here at every size
+  if (!store || q_seq < 0 || store->heads < 0 || store->seq < 0) return H3KV_ERR_INVALID_ARG;
+  if (store->head_dim != H3KV_HEAD_DIM) return H3KV_ERR_UNSUPPORTED;
+  if (q_chunk < 1 || kv_block < 0 || kv_block % H3KV_KV_TILE != 0) return H3KV_ERR_INVALID_ARG;
+  if (store->scale_group == 32) return H3KV_ERR_UNSUPPORTED;
+  if (store->scale_group != 0 && store->scale_group != 128) return H3KV_ERR_INVALID_ARG;
   if (store->heads == 0 || q_seq == 0) return H3KV_OK;
-  // size check first: nothing is touched on the device for a call that does
-  // not fit the fixed scratch
+  // then the fixed scratch: the staging block (rounded up to 256 bytes), then
+  // 8 bytes of row state per (head, query row).  q_seq is bounded before any
+  // product that could wrap; nothing is touched on the device for a call
+  // that does not fit.
   const size_t staging = h3kv_staging_bytes(store->heads, kv_block);
-  if (staging == 0) return H3KV_ERR_INVALID_ARG;
   const size_t staging_aligned = (staging + 255) & ~static_cast<size_t>(255);
-  const size_t state = static_cast<size_t>(store->heads) * static_cast<size_t>(q_seq) * 2 * sizeof(float);
-  if (staging_aligned > H3KV_STATIC_SCRATCH_BYTES || state > H3KV_STATIC_SCRATCH_BYTES - staging_aligned)
+  if (staging == 0 || staging_aligned > H3KV_STATIC_SCRATCH_BYTES) return H3KV_ERR_INVALID_ARG;
+  const size_t row_state_bytes = 2 * sizeof(float) * static_cast<size_t>(store->heads);
+  if (static_cast<uint64_t>(q_seq) > (H3KV_STATIC_SCRATCH_BYTES - staging_aligned) / row_state_bytes)
     return H3KV_ERR_INVALID_ARG;
   void *base = nullptr;
   const h3kv_status st = scratch_address(&base);

@@ -115,3 +115,48 @@ def test_staged_calls_on_two_streams_at_once(cuda):
     b.sync_status(s1)
     b.sync_status(s2)
     assert torch.equal(o1, ref1) and torch.equal(o2, ref2)
+
+
+def test_host_store_buffers_are_all_pinned(cuda):
+    # the staged copies are stream-ordered only from pinned memory; every
+    # buffer of a host store must be page-locked, not only the first of each
+    # kind (an empty_like of a pinned tensor is pageable)
+    b = _b()
+    for sg in (0, 32):
+        st = b.Store.empty(2, 300, host=True, scale_group=sg)
+        assert all(t.is_pinned() for t in (st.k_codes, st.v_codes, st.k_scales, st.v_scales))
+
+
+def test_staged_refuses_a_pageable_store(cuda):
+    # a store buffer in pageable host memory is refused before any copy:
+    # copies from it would take its bytes when issued, not in stream order
+    b = _b()
+    heads, seq = 1, 300
+    q, k, v = synth.make_qkv(heads, seq, seed=61)
+    st = b.Store.empty(heads, seq, host=True)
+    st.v_codes = torch.empty((heads, seq, 128), dtype=torch.int8)  # pageable
+    with pytest.raises(b.H3kvError) as e:
+        b.attend_staged(q.to(cuda), st, q_chunk=256, kv_block=128)
+    assert e.value.status == b.H3KV_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("buffers", [1, 2])
+def test_staged_reads_a_host_store_built_just_before(cuda, buffers):
+    # the store is built into host memory behind a long queue of GPU work and
+    # attended at once, with no synchronisation: the block copies must read
+    # it in stream order, after the build (a pageable buffer was read before
+    # the build ran, and every output row was wrong)
+    b = _b()
+    heads, seq, kvb = 1, 300, 128
+    q, k, v = synth.make_qkv(heads, seq, seed=62, q_seq=200000, device=cuda)
+    ref = b.attend(q, b.build_store(k, v), q_chunk=1 << 16, kv_block=kvb)
+    b.sync_status()
+    x = torch.randn((8192, 8192), device=cuda)
+    for _ in range(40):  # tens of milliseconds of queued work before the build
+        x = (x @ x) * 1e-3
+    host = b.build_store(k, v, out=b.Store.empty(heads, seq, host=True))
+    nbytes = b.h3kv_staging_bytes(heads, kvb) if buffers == 1 else b.staging_bytes_double(heads, kvb)
+    out = b.attend_staged(q, host, q_chunk=1 << 16, kv_block=kvb,
+                          staging=torch.empty(nbytes, dtype=torch.uint8, device=cuda))
+    b.sync_status()
+    assert torch.equal(out, ref)
