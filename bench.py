@@ -41,7 +41,9 @@ HEAD_DIM = 128
 MUFU_EX2_PER_CLK_PER_SM = 32  # ex2 throughput measured on GB300 (a dependent-free MUFU loop)
 KERNEL_SOURCES = ["store_h3kv_build_gb300/csrc/attend.cuh", "store_h3kv_build_gb300/csrc/attend_kvi8r.cu",
                   "store_h3kv_build_gb300/csrc/ptx.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attend_kvi8r_traffic.json")
+BUILD_SOURCES = ["store_h3kv_build_gb300/csrc/store_build.cu", "store_h3kv_build_gb300/csrc/ptx.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attend_kvi8r_traffic_h4_l217088.md")
+BUILD_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "store_build_traffic_h4_l217088.md")
 
 
 def attention_flops(heads, q_seq, kv_seq):
@@ -92,22 +94,47 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def kernel_sha():
+def source_sha(files):
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in files:
         h.update(open(os.path.join(ROOT, f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(launches_per_call):
-    """DRAM bytes per attention launch from the committed ncu summary, if that
-    summary was taken on the current kernel source (else None)."""
-    if not os.path.exists(TRAFFIC_FILE):
+def kernel_sha():
+    return source_sha(KERNEL_SOURCES)
+
+
+def read_summary_values(path):
+    """`key: value` lines of a committed ncu summary (the figures bench.py
+    reports; every other line is prose)."""
+    vals = {}
+    if os.path.exists(path):
+        for ln in open(path):
+            if ln.startswith("- `") and "`: " in ln:
+                k, v = ln[3:].split("`: ", 1)
+                vals[k.strip()] = v.strip().split()[0]
+    return vals
+
+
+def recorded_traffic(heads, seq):
+    """DRAM bytes per full attention launch (16384 query rows x all heads over
+    all keys) from the committed ncu summary, if it was taken on the current
+    kernel source (else None): one launch on 4 heads x 217088 tokens, scaled
+    by heads."""
+    d = read_summary_values(TRAFFIC_FILE)
+    if d.get("kernel_src_sha") != kernel_sha() or int(d.get("seq", 0)) != seq:
         return None
-    d = json.load(open(TRAFFIC_FILE))
-    if d.get("kernel_src_sha") != kernel_sha():
+    return float(d["dram_bytes_per_launch"]) * heads / int(d["heads"])
+
+
+def recorded_build_traffic(heads, seq):
+    """DRAM bytes of one store build from the committed ncu summary (4 heads
+    x 217088 tokens), scaled by rows, if it was taken on the current source."""
+    d = read_summary_values(BUILD_TRAFFIC_FILE)
+    if d.get("kernel_src_sha") != source_sha(BUILD_SOURCES):
         return None
-    return d.get("dram_bytes_per_full_launch")
+    return float(d["dram_bytes_per_call"]) * heads * seq / (int(d["heads"]) * int(d["seq"]))
 
 
 class ClockSampler:
@@ -313,6 +340,24 @@ def run_ours(args, w, name):
             tdist.barrier()
         torch.cuda.synchronize(dev)
 
+    if args.only != "all":
+        # profiler runs: the store once (or W + K builds), then only the
+        # timed kernel, so that a capture holds a few launches of one kernel
+        b.build_store(k, v, out=st)
+        for _ in range(args.warmup + args.steps):
+            if args.only == "attend":
+                b.attend(q, st, q_chunk=q_chunk, kv_block=kv_block, out=out)
+            else:
+                b.build_store(k, v, out=st)
+        b.sync_status()
+        if rank == 0:
+            print(json.dumps({"only": args.only, "workload": name, "steps": args.steps, "warmup": args.warmup}),
+                  flush=True)
+        if dist:
+            import torch.distributed as tdist
+            tdist.destroy_process_group()
+        return 0
+
     for _ in range(args.warmup):
         step()
     b.sync_status()
@@ -475,21 +520,19 @@ def run_ours(args, w, name):
         peaks, peak_src = load_peaks()
         peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
         achieved = flops * args.steps / (attend_sum / 1e3) / 1e12
-        traffic = recorded_traffic(n_chunks)
+        traffic = recorded_traffic(H, L)
         build_gbs = store_bytes(H, L) * args.steps / (build_sum / 1e3) / 1e9
         sm_hz = (clocks.summary().get("sm_mhz") or 0) * 1e6
         n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
         exp_count = H * L * L  # one exp2 per score
         exp_rate = exp_count * args.steps / (attend_sum / 1e3)
         mufu_peak = MUFU_EX2_PER_CLK_PER_SM * n_sms * sm_hz if sm_hz else None
-        line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp16", "data": "synthetic", "config": workload_desc(name, w),
-            "store_build": {"value": build_gbs, "unit": "GB/s", "ms": build_sum / args.steps,
-                            "bytes": store_bytes(H, L), "frac_of_hbm": build_gbs / peaks["hbm_gbs"],
-                            "hbm_peak_gbs": peaks["hbm_gbs"]},
+        store_frac = build_gbs / peaks["hbm_gbs"]
+        detail = {
             "attend_ms": attend_sum / args.steps,
+            "store_build": {"value": build_gbs, "unit": "GB/s", "ms": build_sum / args.steps,
+                            "bytes": store_bytes(H, L), "frac_of_hbm": store_frac,
+                            "hbm_peak_gbs": peaks["hbm_gbs"]},
             "exact_attend": {"ms": exact_ms, "tflops": flops / (exact_ms / 1e3) / 1e12,
                              "kvi8r_over_exact_time": (attend_sum / args.steps) / exact_ms},
             "g32_store": {"what": "one fp16 scale per 32 rotated values",
@@ -519,16 +562,6 @@ def run_ours(args, w, name):
                            "attend_ms": host_attend_ms, "attend_tflops": flops / (host_attend_ms / 1e3) / 1e12,
                            "build_ms": host_build_ms,
                            "build_gbs": store_bytes(H, L) / (host_build_ms / 1e3) / 1e9},
-            "roofline": {"bound": "tensor", "kernel": "attend_kernel<kvi8r>", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak,
-                         "peak_source": f"{peak_src} bf16_tflops_sustained (fp16 dense rate = bf16)",
-                         "frac_of_burst": achieved / peaks["bf16_tflops"],
-                         "traffic": traffic, "launches_per_step": n_chunks,
-                         "flops_per_step": flops},
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps, "clocks": e2e_clocks.summary(),
-                    "api": "h3kv_build_store reading pinned host K, V over NVLink-C2C; h3kv_attend_hostio "
-                           "(pinned host Q in, O out, per query chunk)"},
             "exp": {"count_per_step": exp_count, "per_s": exp_rate, "unit": "exp2/s",
                     "mufu_peak_per_s": mufu_peak, "frac": exp_rate / mufu_peak if mufu_peak else None,
                     "peak_source": f"{MUFU_EX2_PER_CLK_PER_SM} ex2 per clock per SM (measured on GB300) x "
@@ -539,26 +572,63 @@ def run_ours(args, w, name):
                        "note": "the library allocates no device memory: the store, O and any scratch are "
                                "caller-owned; attend_transient_bytes is the measured free-memory change "
                                "around one call"},
+            "e2e_api": "h3kv_build_store reading pinned host K, V over NVLink-C2C; h3kv_attend_hostio "
+                       "(pinned host Q in, O out, per query chunk)",
+            "e2e_clocks": e2e_clocks.summary(),
+            "wall_s_timed": t_wall,
+        }
+        # One compact line on stdout (the record); every comparison path and
+        # the long descriptions go to stderr as a second JSON document.
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
+            "config": {"workload": name, "heads": H, "seq": L, "head_dim": HEAD_DIM, "q_chunk": q_chunk,
+                       "kv_block": kv_block, "k_outliers": w["k_outliers"],
+                       "l2": "no flush: inputs far larger than L2"},
+            "roofline": {"bound": "tensor", "kernel": "attend_kernel<kvi8r>", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "frac_of_burst": achieved / peaks["bf16_tflops"],
+                         "peak_source": f"{peak_src} bf16 sustained", "traffic": traffic,
+                         "store_build": {"bound": "hbm", "kernel": "store_build_kernel", "achieved": build_gbs,
+                                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": store_frac,
+                                         "ms": build_sum / args.steps, "bytes": store_bytes(H, L),
+                                         "traffic": recorded_build_traffic(H, L)}},
+            "paths": {"kvi8r_attend_ms": attend_sum / args.steps,
+                      "exact_tflops": flops / (exact_ms / 1e3) / 1e12,
+                      "kvi8r_over_exact_time": (attend_sum / args.steps) / exact_ms,
+                      "g32_tflops": flops / (g32_attend_ms / 1e3) / 1e12,
+                      "g32_build_gbs": g32_bytes / (g32_build_ms / 1e3) / 1e9,
+                      "f8_tflops": flops / (f8_attend_ms / 1e3) / 1e12,
+                      "f8_build_gbs": f8_bytes / (f8_build_ms / 1e3) / 1e9,
+                      "fp4_tflops": flops / (fp4_attend_ms / 1e3) / 1e12,
+                      "fp4_build_gbs": fp4_bytes / (fp4_build_ms / 1e3) / 1e9,
+                      "host_store_tflops": flops / (host_attend_ms / 1e3) / 1e12,
+                      "attend_transient_bytes": attend_transient},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks.summary(),
-            "wall_s_timed": t_wall,
         }
         if not args.no_cpu_baseline:
             att, gbs, s, desc = time_oracle_sample(w, rows=args.ref_rows)
             line["cpu_baseline"] = {"value": att, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-                                    "sample": desc, "store_gbs": gbs, "seconds": s,
-                                    "os_cpu_count": os.cpu_count(),
-                                    "full_call_s_extrapolated": flops / (att * 1e12) + store_bytes(H, L) / (gbs * 1e9),
-                                    "extrapolation": "the whole workload's attention FLOPs at the sample's FLOP/s "
-                                                     "plus its store bytes at the sample's GB/s (not measured)"}
+                                    "sample": f"1 head x {L} tokens: store, then {args.ref_rows} query rows "
+                                              "over all keys (NumPy fp64)",
+                                    "store_gbs": gbs, "seconds": s}
+            detail["cpu_baseline"] = {"sample": desc, "os_cpu_count": os.cpu_count(),
+                                      "full_call_s_extrapolated": flops / (att * 1e12) + store_bytes(H, L) / (gbs * 1e9),
+                                      "extrapolation": "the whole workload's attention FLOPs at the sample's "
+                                                       "FLOP/s plus its store bytes at the sample's GB/s (not "
+                                                       "measured)"}
             att8, gbs8, s8, desc8 = time_oracle_sample_f8(w)
-            line["f8_store"]["cpu_baseline"] = {"value": att8, "unit": UNIT, "cores": blas_threads(),
-                                                "kind": "oracle", "sample": desc8, "store_gbs": gbs8,
-                                                "seconds": s8}
+            detail["f8_store"]["cpu_baseline"] = {"value": att8, "unit": UNIT, "cores": blas_threads(),
+                                                  "kind": "oracle", "sample": desc8, "store_gbs": gbs8,
+                                                  "seconds": s8}
             att4, gbs4, s4, desc4 = time_oracle_sample_fp4(w)
-            line["fp4_store"]["cpu_baseline"] = {"value": att4, "unit": UNIT, "cores": blas_threads(),
-                                                 "kind": "oracle", "sample": desc4, "store_gbs": gbs4,
-                                                 "seconds": s4}
+            detail["fp4_store"]["cpu_baseline"] = {"value": att4, "unit": UNIT, "cores": blas_threads(),
+                                                   "kind": "oracle", "sample": desc4, "store_gbs": gbs4,
+                                                   "seconds": s4}
+        print(json.dumps({"bench_detail": detail, "config": workload_desc(name, w)}), file=sys.stderr, flush=True)
         print(json.dumps(line), flush=True)
     if dist:
         import torch.distributed as tdist
@@ -577,6 +647,9 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=2048, help="query rows in the oracle's bounded sample")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="omit the oracle timing (used for profiler runs only)")
+    ap.add_argument("--only", choices=["all", "attend", "build"], default="all",
+                    help="profiler runs: time only the kvi8r attention or only the store build, and skip the "
+                         "end-to-end and comparison paths")
     args = ap.parse_args()
     w = synth.WORKLOADS[args.workload]
     if args.impl == "reference":

