@@ -207,8 +207,11 @@ def test_store_f8_v_ties_decided_exactly(cuda):
     #   channels 1-63: absmax 448 * t * 2^-8 for odd t, so s_v = t * 2^-8 is
     #              exact, and values m * s_v for every e4m3 midpoint m that
     #              bf16 holds (exact ties);
-    #   channels 64-127: N(0, 1) bf16 values, where about 1e-3 of the
-    #              quotients land within an fp32 ulp of a boundary.
+    #   channels 64-95: N(0, 1) bf16 values, where about 1e-3 of the
+    #              quotients land within an fp32 ulp of a boundary;
+    #   channels 96-127: one value of 1 and the rest N(0, 1) * 1e-4, so most
+    #              quotients fall in e4m3's subnormal range (below 2^-6), with
+    #              its ties at odd multiples of 2^-10.
     col = [12.25, 0.1708984375, 0.000347137451171875, -0.1708984375, 1.0, 0.5, 7.0 / 256.0, 7.0 / 512.0]
     vals = f8.e4m3_values()[:0x7F]
     mids = (vals[1:] + vals[:-1]) / 2
@@ -224,6 +227,8 @@ def test_store_f8_v_ties_decided_exactly(cuda):
         pick = rng.choice(cand, size=seq - 1) * rng.choice([-1.0, 1.0], size=seq - 1)
         v[0, 0, c] = 448 * s
         v[0, 1:, c] = torch.tensor(pick)
+    v[0, :, 96:] *= 1e-4
+    v[0, 7, 96:] = 1.0
     vb = v.to(torch.bfloat16)
     assert torch.equal(vb.double()[0, :, :64], v[0, :, :64])
     _, k, _ = synth.make_qkv(1, seq, seed=62)
