@@ -341,14 +341,26 @@ def run_ours(args, w, name):
         torch.cuda.synchronize(dev)
 
     if args.only != "all":
-        # profiler runs: the store once (or W + K builds), then only the
-        # timed kernel, so that a capture holds a few launches of one kernel
-        b.build_store(k, v, out=st)
+        # profiler runs: the store once, then W + K calls of only the kernel
+        # asked for, so that a capture holds a few launches of one kernel
+        kind = args.only
+        if kind.endswith("fp4"):
+            sx = b.build_store_fp4(k, v)
+        elif kind.endswith("f8"):
+            sx = b.build_store_f8(k, v)
+        else:
+            sx = b.build_store(k, v, out=st)
+        calls = {
+            "attend": lambda: b.attend(q, sx, q_chunk=q_chunk, kv_block=kv_block, out=out),
+            "attend_exact": lambda: b.attend_exact(q, k, v, q_chunk=q_chunk, kv_block=0, out=out),
+            "attend_fp4": lambda: b.attend_fp4(q, sx, q_chunk=q_chunk, kv_block=kv_block, out=out),
+            "attend_f8": lambda: b.attend_f8(q, sx, q_chunk=q_chunk, kv_block=kv_block, out=out),
+            "build": lambda: b.build_store(k, v, out=sx),
+            "build_fp4": lambda: b.build_store_fp4(k, v, out=sx),
+            "build_f8": lambda: b.build_store_f8(k, v, out=sx),
+        }
         for _ in range(args.warmup + args.steps):
-            if args.only == "attend":
-                b.attend(q, st, q_chunk=q_chunk, kv_block=kv_block, out=out)
-            else:
-                b.build_store(k, v, out=st)
+            calls[kind]()
         b.sync_status()
         if rank == 0:
             print(json.dumps({"only": args.only, "workload": name, "steps": args.steps, "warmup": args.warmup}),
@@ -647,9 +659,11 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=2048, help="query rows in the oracle's bounded sample")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="omit the oracle timing (used for profiler runs only)")
-    ap.add_argument("--only", choices=["all", "attend", "build"], default="all",
-                    help="profiler runs: time only the kvi8r attention or only the store build, and skip the "
-                         "end-to-end and comparison paths")
+    ap.add_argument("--only", default="all",
+                    choices=["all", "attend", "attend_exact", "attend_fp4", "attend_f8", "build", "build_fp4",
+                             "build_f8"],
+                    help="profiler runs: build the store once, then run only the named kernel W + K times "
+                         "(no timing, no end-to-end or comparison paths)")
     args = ap.parse_args()
     w = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
