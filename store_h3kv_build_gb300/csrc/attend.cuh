@@ -150,11 +150,17 @@ __device__ __forceinline__ DqOffsets dq_offsets(int dw, int lane) {
 template <int kGroups>
 __device__ __forceinline__ void dequant_scales(const uint16_t *scales, int valid, int dw, int lane,
                                                uint16_t (&sc)[8]) {
+  // row of iteration it: dw*32 + rr + 4*it (dq_row); one base pointer, the
+  // iterations at immediate offsets; bounds checks only on a ragged tile
+  const int rr = 2 * (lane >> 4) + ((lane >> 2) & 1);
   const int grp = kGroups == 1 ? 0 : static_cast<int>(dq_granule(lane) >> 1);
+  const uint16_t *p = scales + (dw * 32 + rr) * kGroups + grp;
+  if (valid >= kBN) {
 #pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    const int r = static_cast<int>(dq_row(dw, it, lane));
-    sc[it] = r < valid ? __ldcg(scales + r * kGroups + grp) : 0;
+    for (int it = 0; it < 8; ++it) sc[it] = __ldcg(p + it * 4 * kGroups);
+  } else {
+#pragma unroll
+    for (int it = 0; it < 8; ++it) sc[it] = dw * 32 + rr + 4 * it < valid ? __ldcg(p + it * 4 * kGroups) : 0;
   }
 }
 
@@ -201,13 +207,18 @@ __device__ __forceinline__ void dequant16_fp4(const uint2 raw, uint32_t s2, uint
 // words for iteration `it`; rows past `valid` get 0.
 __device__ __forceinline__ void dequant_scales_fp4(const uint8_t *scales, int valid, int dw, int lane,
                                                    uint32_t (&sc)[2]) {
-  const int g = static_cast<int>(dq_granule(lane));
+  const int rr = 2 * (lane >> 4) + ((lane >> 2) & 1);
+  const uint8_t *p = scales + (dw * 32 + rr) * 8 + static_cast<int>(dq_granule(lane));
   sc[0] = sc[1] = 0u;
+  if (valid >= kBN) {
 #pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    const int r = static_cast<int>(dq_row(dw, it, lane));
-    const uint32_t b = r < valid ? __ldcg(scales + r * 8 + g) : 0u;
-    sc[it >> 2] |= b << ((it & 3) * 8);
+    for (int it = 0; it < 8; ++it) sc[it >> 2] |= static_cast<uint32_t>(__ldcg(p + it * 32)) << ((it & 3) * 8);
+  } else {
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const uint32_t b = dw * 32 + rr + 4 * it < valid ? __ldcg(p + it * 32) : 0u;
+      sc[it >> 2] |= b << ((it & 3) * 8);
+    }
   }
 }
 
@@ -364,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_b = 0.f, l_b = 0.f;  // current block: running max (raw score units) and sum
     float M = 0.f, Lam = 0.f;    // blocks merged so far
     bool ok = true;
+    int jb = 0;                  // position of tile j in its kv_block (j % blk, by a counter)
     for (int j = 0; j < n_tiles; ++j) {
       if (!warp_wait(smem_u32(&sm.s_full[q]), j & 1, wctx)) {
         ok = false;
@@ -393,11 +405,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mt = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
       }
 
-      if (j % blk == 0) {
+      if (jb == 0) {
         if (j > 0) {
           // merge the finished block (O_q, m_b, l_b) into (M, Lam, O row in
           // global memory, rotated basis, un-normalised)
-          const bool first = (j / blk) == 1;
+          const bool first = j == blk;
           float al = 0.f, be = 1.f;
           if (!first) {
             lse_merge(M, Lam, m_b, l_b, c2, al, be);
@@ -473,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[q]));
       const float2 acc = __fadd2_rn(acc0, acc1);
       l_b += acc.x + acc.y;
+      jb = jb + 1 == blk ? 0 : jb + 1;
     }
 
     if (ok && warp_wait(smem_u32(&sm.o_full), 0, wctx)) {
@@ -592,22 +605,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t *vsc = a.v_fp4_scales + static_cast<int64_t>(h) * a.kv_stride * 8;
       uint32_t sck[2], scv[2];
       const DqOffsets off = dq_offsets(dw, lane);
+      // ring slots and phases, and the scales of tile j, advanced by counters
+      int ks = 0, vs = 0;
+      uint32_t kph = 0, vph = 0;
+      const uint8_t *kst = ksc, *vst = vsc;
+      int64_t left = a.kv_seq;
       for (int j = 0; j < n_tiles; ++j) {
-        const int64_t tok0 = static_cast<int64_t>(j) * kBN;
-        const int valid = static_cast<int>(a.kv_seq - tok0 < kBN ? a.kv_seq - tok0 : kBN);
-        const int ks = j % kNK, vs = j % kNV;
-        dequant_scales_fp4(ksc + tok0 * 8, valid, dw, lane, sck);
-        dequant_scales_fp4(vsc + tok0 * 8, valid, dw, lane, scv);
-        if (!dequant_tile_fp4(sm.k[ks], warp_wait(smem_u32(&sm.k_load[ks]), (j / kNK) & 1, wctx), sck, off))
-          break;
+        const int valid = static_cast<int>(left < kBN ? left : kBN);
+        dequant_scales_fp4(kst, valid, dw, lane, sck);
+        dequant_scales_fp4(vst, valid, dw, lane, scv);
+        if (!dequant_tile_fp4(sm.k[ks], warp_wait(smem_u32(&sm.k_load[ks]), kph, wctx), sck, off)) break;
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sm.k_ready[ks]));
-        if (!dequant_tile_fp4(sm.v[vs], warp_wait(smem_u32(&sm.v_load[vs]), (j / kNV) & 1, wctx), scv, off))
-          break;
+        if (!dequant_tile_fp4(sm.v[vs], warp_wait(smem_u32(&sm.v_load[vs]), vph, wctx), scv, off)) break;
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sm.v_ready[vs]));
+        kst += kBN * 8;
+        vst += kBN * 8;
+        left -= kBN;
+        if (++ks == kNK) {
+          ks = 0;
+          kph ^= 1u;
+        }
+        if (++vs == kNV) {
+          vs = 0;
+          vph ^= 1u;
+        }
       }
     } else if constexpr (kKvi8r) {
       const int dw = warp - 8;
@@ -615,23 +640,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint16_t *vsc = a.v_scales + static_cast<int64_t>(h) * a.kv_stride * kGroups;
       uint16_t sck[8], scv[8];
       const DqOffsets off = dq_offsets(dw, lane);
+      // ring slots and phases, and the scales of tile j, advanced by counters
+      int ks = 0, vs = 0;
+      uint32_t kph = 0, vph = 0;
+      const uint16_t *kst = ksc, *vst = vsc;
+      int64_t left = a.kv_seq;
       for (int j = 0; j < n_tiles; ++j) {
-        const int64_t tok0 = static_cast<int64_t>(j) * kBN;
-        const int valid = static_cast<int>(a.kv_seq - tok0 < kBN ? a.kv_seq - tok0 : kBN);
-        const int ks = j % kNK, vs = j % kNV;
+        const int valid = static_cast<int>(left < kBN ? left : kBN);
         // scale loads go out before the waits so their latency hides there
-        dequant_scales<kGroups>(ksc + tok0 * kGroups, valid, dw, lane, sck);
-        dequant_scales<kGroups>(vsc + tok0 * kGroups, valid, dw, lane, scv);
-        if (!warp_wait(smem_u32(&sm.k_load[ks]), (j / kNK) & 1, wctx)) break;
+        dequant_scales<kGroups>(kst, valid, dw, lane, sck);
+        dequant_scales<kGroups>(vst, valid, dw, lane, scv);
+        if (!warp_wait(smem_u32(&sm.k_load[ks]), kph, wctx)) break;
         dequant_tile(sm.k[ks], sck, off);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sm.k_ready[ks]));
-        if (!warp_wait(smem_u32(&sm.v_load[vs]), (j / kNV) & 1, wctx)) break;
+        if (!warp_wait(smem_u32(&sm.v_load[vs]), vph, wctx)) break;
         dequant_tile(sm.v[vs], scv, off);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sm.v_ready[vs]));
+        kst += kBN * kGroups;
+        vst += kBN * kGroups;
+        left -= kBN;
+        if (++ks == kNK) {
+          ks = 0;
+          kph ^= 1u;
+        }
+        if (++vs == kNV) {
+          vs = 0;
+          vph ^= 1u;
+        }
       }
     }
   } else {

@@ -164,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_b = 0.f, l_b = 0.f;  // current kv_block: running max and sum of the (scaled) weights
     float M = 0.f, Lam = 0.f;    // blocks merged so far
     bool ok = true;
+    int jb = 0;                  // position of tile j in its kv_block (j % blk, by a counter)
     for (int j = 0; j < n_tiles; ++j) {
       // the tile's two K block scales (loaded before the wait hides their latency)
       const int b0 = 2 * j;
@@ -198,11 +199,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mt = fmaxf(fmaxf(h0[0], h0[1]) * mult0, fmaxf(h1[0], h1[1]) * mult1);
       }
 
-      if (j % blk == 0) {
+      if (jb == 0) {
         if (j > 0) {
           // merge the finished kv_block (O_q, m_b, l_b) into (M, Lam, O row
           // in global memory, un-normalised)
-          const bool first = (j / blk) == 1;
+          const bool first = j == blk;
           float al = 0.f, be = 1.f;
           if (!first) {
             attn::lse_merge(M, Lam, m_b, l_b, 1.0f, al, be);
@@ -281,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[q]));
       const float2 acc = __fadd2_rn(acc0, acc1);
       l_b += acc.x + acc.y;
+      jb = jb + 1 == blk ? 0 : jb + 1;
     }
 
     if (ok && attn::warp_wait(smem_u32(&sm.o_full), 0, wctx)) {
