@@ -378,67 +378,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kNV; ++s)
           if (v_issued[s]) mbar_wait_drain(smem_u32(&sm.v_full[s]), (v_issued[s] - 1) & 1, kDrainNs);
       }
-    } else if (warp == 13 && lane == 0) {
+    } else if (warp == 13) {
       // ====================================================== MMA issuer
+      // the whole warp runs the loop and waits (warp-uniform operands); one
+      // elected lane issues each MMA and commit
+      const uint32_t go = elect_one();
       constexpr uint32_t idesc = idesc_e4m3(kBM, 128);
       // K-major 128-byte-swizzled operands; one K step (32 codes = 32 bytes)
-      // advances the start address by 32 bytes (2 in the >>4 field)
+      // advances the start address by 32 bytes (2 in the >>4 field of the
+      // low word); the three descriptors share the high word
       const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
-      const uint64_t dk0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
-      const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[0]), 16, 1024);
+      const uint32_t dhi = static_cast<uint32_t>(dq0 >> 32);
+      const uint32_t lq0 = static_cast<uint32_t>(dq0);
+      const uint32_t lk0 = static_cast<uint32_t>(sdesc_sw128(smem_u32(sm.k[0]), 16, 1024));
+      const uint32_t lv0 = static_cast<uint32_t>(sdesc_sw128(smem_u32(sm.v[0]), 16, 1024));
       auto issue_qk = [&](int q, int ks) {
-        const uint64_t dq = dq0 + static_cast<uint64_t>(q * (kTile8 >> 4));
-        const uint64_t dk = dk0 + static_cast<uint64_t>(ks * (kTile8 >> 4));
+        const uint32_t lq = lq0 + q * (kTile8 >> 4);
+        const uint32_t lk = lk0 + ks * (kTile8 >> 4);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_ss_f8(tmem + q * 128, dq + 2 * kk, dk + 2 * kk, idesc, kk > 0);
+        for (int kk = 0; kk < 4; ++kk) mma_ss_f8(go, tmem + q * 128, lq + 2 * kk, lk + 2 * kk, dhi, idesc, kk > 0);
       };
       auto issue_pv = [&](int q, int vs, bool acc) {
-        const uint64_t dv = dv0 + static_cast<uint64_t>(vs * (kTile8 >> 4));
+        const uint32_t lv = lv0 + vs * (kTile8 >> 4);
         // P: 32 keys per step = 8 TMEM columns of four e4m3 values
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_ts_f8(tmem + 256 + q * 128, tmem + q * 128 + kk * 8, dv + 2 * kk, idesc, (acc || kk > 0) ? 1u : 0u);
+          mma_ts_f8(go, tmem + 256 + q * 128, tmem + q * 128 + kk * 8, lv + 2 * kk, dhi, idesc,
+                    (acc || kk > 0) ? 1u : 0u);
       };
-      bool ok = mbar_wait(smem_u32(&sm.q_full), 0, wctx) && mbar_wait(smem_u32(&sm.k_full[0]), 0, wctx);
+      bool ok = attn::warp_wait(smem_u32(&sm.q_full), 0, wctx) && attn::warp_wait(smem_u32(&sm.k_full[0]), 0, wctx);
       if (ok) {
         tc_fence_after();
         issue_qk(0, 0);
-        mma_commit(smem_u32(&sm.s_full[0]));
+        mma_commit(go, smem_u32(&sm.s_full[0]));
         issue_qk(1, 0);
-        mma_commit(smem_u32(&sm.s_full[1]));
-        mma_commit(smem_u32(&sm.k_free[0]));
+        mma_commit(go, smem_u32(&sm.s_full[1]));
+        mma_commit(go, smem_u32(&sm.k_free[0]));
         int jb = 0;  // j mod kv_block_tiles, kept by a counter (no division in the issue loop)
         for (int j = 0; j < n_tiles && ok; ++j) {
           const int vs = j % kNV;
           const bool acc = jb != 0;
           const bool more = j + 1 < n_tiles;
           const int ks1 = (j + 1) % kNK;
-          ok = mbar_wait(smem_u32(&sm.v_full[vs]), (j / kNV) & 1, wctx) &&
-               mbar_wait(smem_u32(&sm.p_full[0]), j & 1, wctx);
+          ok = attn::warp_wait(smem_u32(&sm.v_full[vs]), (j / kNV) & 1, wctx) &&
+               attn::warp_wait(smem_u32(&sm.p_full[0]), j & 1, wctx);
           if (!ok) break;
           tc_fence_after();
           issue_pv(0, vs, acc);
           if (more) {
-            if (!(ok = mbar_wait(smem_u32(&sm.k_full[ks1]), ((j + 1) / kNK) & 1, wctx))) break;
+            if (!(ok = attn::warp_wait(smem_u32(&sm.k_full[ks1]), ((j + 1) / kNK) & 1, wctx))) break;
             tc_fence_after();
             issue_qk(0, ks1);
-            mma_commit(smem_u32(&sm.s_full[0]));
+            mma_commit(go, smem_u32(&sm.s_full[0]));
           }
-          if (!(ok = mbar_wait(smem_u32(&sm.p_full[1]), j & 1, wctx))) break;
+          if (!(ok = attn::warp_wait(smem_u32(&sm.p_full[1]), j & 1, wctx))) break;
           tc_fence_after();
           issue_pv(1, vs, acc);
-          mma_commit(smem_u32(&sm.v_free[vs]));
+          mma_commit(go, smem_u32(&sm.v_free[vs]));
           if (more) {
             issue_qk(1, ks1);
-            mma_commit(smem_u32(&sm.s_full[1]));
-            mma_commit(smem_u32(&sm.k_free[ks1]));
+            mma_commit(go, smem_u32(&sm.s_full[1]));
+            mma_commit(go, smem_u32(&sm.k_free[ks1]));
           }
           jb = jb + 1 == blk ? 0 : jb + 1;
         }
-        if (ok) mma_commit(smem_u32(&sm.o_full));
+        if (ok) mma_commit(go, smem_u32(&sm.o_full));
       }
       // every MMA issued must finish before TMEM is released
-      mma_commit(smem_u32(&sm.drain));
+      mma_commit(go, smem_u32(&sm.drain));
       mbar_wait_drain(smem_u32(&sm.drain), 0, kDrainNs);
     }
   }

@@ -264,25 +264,50 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool b_mn_major, uin
          ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
-// D(tmem) (+)= A(smem desc) * B(smem desc)
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                       uint32_t accumulate) {
+// One lane of a converged warp (elect.sync over the full mask): 1 there, 0
+// in the other lanes.
+__device__ __forceinline__ uint32_t elect_one() {
+  uint32_t r;
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .b32 l;\n\t.reg .pred p;\n\t"
+      "elect.sync l|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r));
+  return r;
+}
+
+// tcgen05.mma is issued by one thread.  The helpers below are called by a
+// whole converged warp, so that every operand is computed warp-uniformly, and
+// only the lanes whose `go` is nonzero (one elected lane) issue.  A shared-
+// memory descriptor is passed as its low word (start address >> 4 and leading
+// byte offset) plus a high word (stride byte offset, version, swizzle) that
+// all operands of a kernel share; the 64-bit descriptor is put together in
+// the instruction's own block.
+
+// D(tmem) (+)= A(smem desc) * B(smem desc), kind::f16
+__device__ __forceinline__ void mma_ss(uint32_t go, uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, g;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %3};\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "setp.ne.b32 g, %6, 0;\n\t"
+      "@g tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate), "r"(go)
       : "memory");
 }
 
-// D(tmem) (+)= A(tmem) * B(smem desc)
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                       uint32_t accumulate) {
+// D(tmem) (+)= A(tmem) * B(smem desc), kind::f16
+__device__ __forceinline__ void mma_ts(uint32_t go, uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                       uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p, g;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "setp.ne.b32 g, %6, 0;\n\t"
+      "@g tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate), "r"(go)
       : "memory");
 }
 
@@ -294,24 +319,29 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(uint32_t m, uint32_t n) {
 }
 
 // D(tmem) (+)= A(smem desc) * B(smem desc), 8-bit operands (K = 32 per op)
-__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate) {
+__device__ __forceinline__ void mma_ss_f8(uint32_t go, uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p, g;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %3};\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "setp.ne.b32 g, %6, 0;\n\t"
+      "@g tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate), "r"(go)
       : "memory");
 }
 
 // D(tmem) (+)= A(tmem, four 8-bit values per column) * B(smem desc)
-__device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate) {
+__device__ __forceinline__ void mma_ts_f8(uint32_t go, uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p, g;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "setp.ne.b32 g, %6, 0;\n\t"
+      "@g tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate), "r"(go)
       : "memory");
 }
 
@@ -326,10 +356,15 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 // completion in stream order.
 __device__ __forceinline__ void pdl_wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// Arrive once on `bar` when every prior tcgen05 async op of this thread is done.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
+// Arrive once on `bar` when every prior tcgen05 async op of the issuing
+// thread is done; issued by the lanes whose `go` is nonzero (as the MMAs).
+__device__ __forceinline__ void mma_commit(uint32_t go, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred g;\n\t"
+      "setp.ne.b32 g, %1, 0;\n\t"
+      "@g tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+      "r"(go)
+      : "memory");
 }
 
 // 32 lanes x 32 columns of 32-bit TMEM -> 32 registers per thread, then wait.
