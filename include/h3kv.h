@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define H3KV_ABI_VERSION 5u
+#define H3KV_ABI_VERSION 6u
 #define H3KV_HEAD_DIM 128
 /* kv_block = 0 on the kvi8r path means this many tokens (the kv_block
  * default of the kv_store row). */
@@ -334,8 +334,21 @@ h3kv_status h3kv_sync_status(void *stream);
  * launches; 0 restores the default of 1 s.  Process-wide.  A limit far below
  * the kernels' normal waits makes them give up early: the launch then
  * records H3KV_ERR_DEVICE_TIMEOUT, drains its own copies and MMAs, and exits
- * with its output undefined, leaving the context usable. */
+ * with its output undefined, leaving the context usable.  A wait whose
+ * phase completes while its first (suspended) poll is pending never runs
+ * out, however small the limit (see h3kv_debug_withhold_p). */
 h3kv_status h3kv_set_wait_timeout_ns(uint64_t timeout_ns);
+
+/* Diagnostic of the failure path (no counterpart on the pages): in later
+ * attention launches (every path), the softmax warps of every CTA withhold
+ * their "P ready" arrival for the 128-key tile `tile` of the launch (counted
+ * from 0 within each launch), so that the MMA warp's bounded wait for it runs
+ * out: the launch records H3KV_ERR_DEVICE_TIMEOUT, drains its copies and
+ * MMAs and exits, its output undefined.  -1 (the default) withholds nothing;
+ * below -1: H3KV_ERR_INVALID_ARG.  Process-wide.  A suspended barrier poll
+ * can outlast a tiny wait limit, so a small limit alone does not make every
+ * kernel give up; a wait on an arrival that never comes always runs out. */
+h3kv_status h3kv_debug_withhold_p(int32_t tile);
 
 /* Diagnostic of the failure path (no counterpart on the pages): launch one
  * CTA whose only wait is on a barrier that nothing ever arrives on, limited

@@ -20,6 +20,7 @@ __device__ uint32_t g_h3kv_error;
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s per bounded wait
 std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
+std::atomic<int32_t> g_withhold_p_tile1{0};  // diagnostic, see h3kv_debug_withhold_p
 
 // One CTA waits on an mbarrier that nothing ever arrives on: the bounded wait
 // runs out, records the timeout in the device error word and the kernel
@@ -251,6 +252,7 @@ h3kv_status h3kv_attend(const uint16_t *Q, int64_t q_seq, const h3kv_store *stor
   a.scale_log2 = scale_log2_of(softmax_scale);
   a.err = d->err;
   a.timeout_ns = g_timeout_ns.load();
+  a.withhold_p_tile1 = g_withhold_p_tile1.load();
   for (int64_t c0 = 0; c0 < q_seq; c0 += q_chunk) {
     a.q_begin = c0;
     a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
@@ -294,6 +296,7 @@ h3kv_status h3kv_attend_exact(const uint16_t *Q, int64_t q_seq, const uint16_t *
   a.scale_log2 = scale_log2_of(softmax_scale);
   a.err = d->err;
   a.timeout_ns = g_timeout_ns.load();
+  a.withhold_p_tile1 = g_withhold_p_tile1.load();
   for (int64_t c0 = 0; c0 < q_seq; c0 += q_chunk) {
     a.q_begin = c0;
     a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
@@ -363,6 +366,7 @@ h3kv_status h3kv_attend_staged(const uint16_t *Q, int64_t q_seq, const h3kv_stor
   a.scale_log2 = scale_log2_of(softmax_scale);
   a.err = d->err;
   a.timeout_ns = g_timeout_ns.load();
+  a.withhold_p_tile1 = g_withhold_p_tile1.load();
   a.state = reinterpret_cast<float2 *>(state);
   a.scale_groups = 1;
   const int64_t n_blocks = (store->seq + kvb - 1) / kvb;
@@ -519,6 +523,7 @@ h3kv_status h3kv_attend_hostio(const uint16_t *Q_host, int64_t q_seq, const h3kv
   a.scale_log2 = scale_log2_of(softmax_scale);
   a.err = d->err;
   a.timeout_ns = g_timeout_ns.load();
+  a.withhold_p_tile1 = g_withhold_p_tile1.load();
   a.q_begin = 0;
 
   // Schedule.  Copy stream cs: reset both ready words, Q chunks 0 and 1 in;
@@ -663,6 +668,7 @@ h3kv_status h3kv_attend_f8(const uint16_t *Q, int64_t q_seq, const h3kv_store_f8
   a.scale_log2 = scale_log2_of(softmax_scale);
   a.err = d->err;
   a.timeout_ns = g_timeout_ns.load();
+  a.withhold_p_tile1 = g_withhold_p_tile1.load();
   for (int64_t c0 = 0; c0 < q_seq; c0 += q_chunk) {
     a.q_begin = c0;
     a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
@@ -738,6 +744,7 @@ h3kv_status h3kv_attend_fp4(const uint16_t *Q, int64_t q_seq, const h3kv_store_f
   a.scale_log2 = scale_log2_of(softmax_scale);
   a.err = d->err;
   a.timeout_ns = g_timeout_ns.load();
+  a.withhold_p_tile1 = g_withhold_p_tile1.load();
   for (int64_t c0 = 0; c0 < q_seq; c0 += q_chunk) {
     a.q_begin = c0;
     a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
@@ -749,6 +756,12 @@ h3kv_status h3kv_attend_fp4(const uint16_t *Q, int64_t q_seq, const h3kv_store_f
 
 h3kv_status h3kv_set_wait_timeout_ns(uint64_t timeout_ns) {
   g_timeout_ns.store(timeout_ns == 0 ? kDefaultTimeoutNs : timeout_ns);
+  return H3KV_OK;
+}
+
+h3kv_status h3kv_debug_withhold_p(int32_t tile) {
+  if (tile < -1) return H3KV_ERR_INVALID_ARG;
+  g_withhold_p_tile1.store(tile + 1);
   return H3KV_OK;
 }
 

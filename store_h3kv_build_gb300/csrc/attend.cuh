@@ -482,7 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[q]));
+      // (a diagnostic may withhold one tile's arrival: see withhold_p_tile1)
+      if (lane == 0 && j + 1 != a.withhold_p_tile1) mbar_arrive(smem_u32(&sm.p_full[q]));
       const float2 acc = __fadd2_rn(acc0, acc1);
       l_b += acc.x + acc.y;
       jb = jb + 1 == blk ? 0 : jb + 1;
@@ -675,8 +676,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     reg_dealloc<kKvi8r ? kRegIssueKvi8r : kRegIssueExact>();
-    if (warp == 12 && lane == 0) {
+    if (warp == 12) {
       // ========================================================== producer
+      // the whole warp waits; one elected lane issues the copies
+      const uint32_t go = elect_one();
       int k_issued[kNK] = {0, 0, 0};
       int v_issued[kNV] = {0, 0};
       if constexpr (!kKvi8r) {
@@ -684,8 +687,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         const uint32_t bar = smem_u32(&sm.q_full);
-        mbar_arrive_expect_tx(bar, kNQ * kTileBytes);
-        for (int q = 0; q < kNQ; ++q)
+        if (go) mbar_arrive_expect_tx(bar, kNQ * kTileBytes);
+        if (go) for (int q = 0; q < kNQ; ++q)
           for (int c = 0; c < 2; ++c)
             tma_load_3d(smem_u32(sm.q[q] + c * kChunkBytes), &tm_q, c * 64, static_cast<int32_t>(row0 + q * kBM),
                         h, bar);
@@ -693,8 +696,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n_tiles; ++j) {
         const int64_t tok0 = static_cast<int64_t>(j) * kBN;
         const int ks = j % kNK, vs = j % kNV;
-        if (!mbar_wait(smem_u32(&sm.k_free[ks]), ((j / kNK) & 1) ^ 1, wctx)) break;
-        {
+        if (!warp_wait(smem_u32(&sm.k_free[ks]), ((j / kNK) & 1) ^ 1, wctx)) break;
+        if (go) {
           const uint32_t bar = smem_u32(&sm.k_load[ks]);
           if constexpr (kFp4) {
             const uint32_t bytes = static_cast<uint32_t>((a.kv_seq - tok0 < kBN ? a.kv_seq - tok0 : kBN) * 64);
@@ -710,10 +713,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(smem_u32(sm.k[ks]), &tm_k, 0, static_cast<int32_t>(tok0), h, bar);
             tma_load_3d(smem_u32(sm.k[ks] + kChunkBytes), &tm_k, 64, static_cast<int32_t>(tok0), h, bar);
           }
-          ++k_issued[ks];
         }
-        if (!mbar_wait(smem_u32(&sm.v_free[vs]), ((j / kNV) & 1) ^ 1, wctx)) break;
-        {
+        ++k_issued[ks];
+        if (!warp_wait(smem_u32(&sm.v_free[vs]), ((j / kNV) & 1) ^ 1, wctx)) break;
+        if (go) {
           const uint32_t bar = smem_u32(&sm.v_load[vs]);
           if constexpr (kFp4) {
             const uint32_t bytes = static_cast<uint32_t>((a.kv_seq - tok0 < kBN ? a.kv_seq - tok0 : kBN) * 64);
@@ -729,8 +732,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(smem_u32(sm.v[vs]), &tm_v, 0, static_cast<int32_t>(tok0), h, bar);
             tma_load_3d(smem_u32(sm.v[vs] + kChunkBytes), &tm_v, 64, static_cast<int32_t>(tok0), h, bar);
           }
-          ++v_issued[vs];
         }
+        ++v_issued[vs];
       }
       if (sm.abort) {
         // every copy this thread issued must land before the CTA exits

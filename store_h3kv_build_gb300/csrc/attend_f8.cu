@@ -279,7 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[q]));
+      // (a diagnostic may withhold one tile's arrival: see withhold_p_tile1)
+      if (lane == 0 && j + 1 != a.withhold_p_tile1) mbar_arrive(smem_u32(&sm.p_full[q]));
       const float2 acc = __fadd2_rn(acc0, acc1);
       l_b += acc.x + acc.y;
       jb = jb + 1 == blk ? 0 : jb + 1;
@@ -347,8 +348,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     reg_dealloc<kRegIdle>();
   } else {
     reg_dealloc<kRegIssue>();
-    if (warp == 12 && lane == 0) {
+    if (warp == 12) {
       // ========================================================== producer
+      // the whole warp waits; one elected lane issues the copies
+      const uint32_t go = elect_one();
       int k_issued[kNK] = {};
       int v_issued[kNV] = {};
       prefetch_tmap(&tm_k);
@@ -356,20 +359,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n_tiles; ++j) {
         const int32_t tok0 = j * kBN;
         const int ks = j % kNK, vs = j % kNV;
-        if (!mbar_wait(smem_u32(&sm.k_free[ks]), ((j / kNK) & 1) ^ 1, wctx)) break;
-        {
+        if (!attn::warp_wait(smem_u32(&sm.k_free[ks]), ((j / kNK) & 1) ^ 1, wctx)) break;
+        if (go) {
           const uint32_t bar = smem_u32(&sm.k_full[ks]);
           mbar_arrive_expect_tx(bar, kTile8);
           tma_load_3d(smem_u32(sm.k[ks]), &tm_k, 0, tok0, h, bar);
-          ++k_issued[ks];
         }
-        if (!mbar_wait(smem_u32(&sm.v_free[vs]), ((j / kNV) & 1) ^ 1, wctx)) break;
-        {
+        ++k_issued[ks];
+        if (!attn::warp_wait(smem_u32(&sm.v_free[vs]), ((j / kNV) & 1) ^ 1, wctx)) break;
+        if (go) {
           const uint32_t bar = smem_u32(&sm.v_full[vs]);
           mbar_arrive_expect_tx(bar, kTile8);
           tma_load_3d(smem_u32(sm.v[vs]), &tm_v, tok0, 0, h, bar);
-          ++v_issued[vs];
         }
+        ++v_issued[vs];
       }
       if (sm.abort) {
         // every copy this thread issued must land before the CTA exits

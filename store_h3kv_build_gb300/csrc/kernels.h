@@ -69,6 +69,10 @@ struct AttnArgs {
   // free; nullptr: no wait.
   const uint32_t *q_ready;
   uint32_t q_ready_value;
+  // Failure-path diagnostic: 1 + the 128-key tile of each launch whose P-ready
+  // arrival the softmax warps withhold, so that the MMA warp's wait for it
+  // runs out; 0 (the default) withholds nothing.
+  int32_t withhold_p_tile1;
 };
 
 constexpr int kAttnRowsPerCta = 256;  // two 128-row query tiles per CTA
@@ -120,6 +124,7 @@ struct F8Args {
   float scale_log2;         // softmax_scale * log2(e)
   uint32_t *err;
   uint64_t timeout_ns;
+  int32_t withhold_p_tile1;  // as AttnArgs::withhold_p_tile1
 };
 
 // kvf8s attention over [q_begin, q_end): K codes through a 3-D map {128,

@@ -21,7 +21,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported():
     names = declared_functions()
-    assert len(names) == 21
+    assert len(names) == 22
     assert {"h3kv_attend_f8", "h3kv_build_store_f8", "h3kv_f8_v_stride", "h3kv_store_f8_bytes"} <= set(names)
     assert {"h3kv_attend_fp4", "h3kv_build_store_fp4", "h3kv_store_fp4_bytes"} <= set(names)
     lib = ctypes.CDLL(b.LIB_PATH)
@@ -31,7 +31,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_abi_version_and_strings():
-    assert b.h3kv_abi_version() == 5
+    assert b.h3kv_abi_version() == 6
     for st in range(5):
         assert b.h3kv_strerror(st)
     assert b.h3kv_strerror(99) == b"unknown status"
@@ -94,6 +94,12 @@ def test_binding_raises_on_error_status():
 def test_wait_timeout_setter_needs_no_device():
     assert b.h3kv_set_wait_timeout_ns(5000) == b.H3KV_OK
     assert b.h3kv_set_wait_timeout_ns(0) == b.H3KV_OK
+
+
+def test_withhold_p_setter_needs_no_device():
+    assert b.h3kv_debug_withhold_p(0) == b.H3KV_OK
+    assert b.h3kv_debug_withhold_p(-1) == b.H3KV_OK
+    assert b.h3kv_debug_withhold_p(-2) == b.H3KV_ERR_INVALID_ARG
 
 
 def test_staging_bytes():
