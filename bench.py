@@ -42,7 +42,7 @@ MUFU_EX2_PER_CLK_PER_SM = 32  # ex2 throughput measured on GB300 (a dependent-fr
 KERNEL_SOURCES = ["store_h3kv_build_gb300/csrc/attend.cuh", "store_h3kv_build_gb300/csrc/attend_kvi8r.cu",
                   "store_h3kv_build_gb300/csrc/ptx.cuh"]
 BUILD_SOURCES = ["store_h3kv_build_gb300/csrc/store_build.cu", "store_h3kv_build_gb300/csrc/ptx.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attend_kvi8r_traffic_h4_l217088.md")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attend_kvi8r_traffic_h32_l217088.md")
 BUILD_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "store_build_traffic_h4_l217088.md")
 
 
@@ -120,8 +120,8 @@ def read_summary_values(path):
 def recorded_traffic(heads, seq):
     """DRAM bytes per full attention launch (16384 query rows x all heads over
     all keys) from the committed ncu summary, if it was taken on the current
-    kernel source (else None): one launch on 4 heads x 217088 tokens, scaled
-    by heads."""
+    kernel source and sequence (else None); scaled by heads if the capture
+    holds fewer heads than the call."""
     d = read_summary_values(TRAFFIC_FILE)
     if d.get("kernel_src_sha") != kernel_sha() or int(d.get("seq", 0)) != seq:
         return None
