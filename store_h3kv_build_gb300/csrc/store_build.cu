@@ -143,10 +143,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
       const int s = it % kStages;
       const uint32_t ph = (it / kStages) & 1;
-      // every compute thread takes the same decision (a wait that gave up on
-      // one thread stops all of them together)
-      const bool ok = mbar_wait(smem_u32(&sm.full[s]), ph, wctx);
-      if (!named_bar_and(1, kRows, ok)) break;
+      // each warp decides for itself (a warp whose wait gave up leaves; the
+      // others see the abort flag at their next wait, and the producer's wait
+      // for the stage's release runs out)
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.full[s]), ph, wctx))) break;
 
       // read my row: element e at chunk e/64, granule (e%64)/8, swizzled
       float x[128];
