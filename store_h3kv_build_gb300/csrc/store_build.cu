@@ -7,21 +7,26 @@
 // GB300 design: HBM-bound stream.  Rows are flattened over heads (each row is
 // independent).  A persistent grid of CTAs (two per SM) walks 128-row tiles;
 // one producer warp streams bf16 tiles into a 3-stage shared-memory ring with
-// TMA (128-byte swizzle), and four compute warps own one row per thread (the
-// swizzle makes the per-row shared-memory reads bank-conflict free), run the
-// 128-point FWHT in registers, and store each row's codes (four 32-byte
-// stores when the code buffers are 32-byte aligned, else eight 16-byte ones)
-// and scale straight from registers.
+// TMA (128-byte swizzle), and eight compute warps give every row two threads
+// (the swizzle makes the per-row shared-memory reads bank-conflict free).
+// H128 = [[H64, H64], [H64, -H64]], so each thread forms the sums (or the
+// differences) of the row's two 64-value halves and runs a 64-point FWHT in
+// registers: 88 registers, 18 warps per SM instead of 10 with one row per
+// thread.  Each thread stores its half row's codes (two 32-byte stores when
+// the code buffers are 32-byte aligned, else four 16-byte ones); the pair
+// shares its absmax with one shuffle.
 #include "kernels.h"
 #include "ptx.cuh"
 
 namespace h3kv {
 namespace {
 
-constexpr int kRows = 128;                  // rows per tile = compute threads
+constexpr int kRows = 128;                  // rows per tile
+constexpr int kCompute = 2 * kRows;         // two compute threads per row
 constexpr int kStages = 3;                  // input ring depth (2 CTAs per SM, 97 KB each)
 constexpr int kInTileBytes = kRows * 256;   // bf16 [128 x 128]
-constexpr int kThreads = kRows + 32;        // 4 compute warps + 1 producer warp
+constexpr int kThreads = kCompute + 32;     // 8 compute warps + 1 producer warp
+constexpr int kProducerWarp = kCompute / 32;
 
 struct BuildSmem {
   // 1024-byte aligned tiles first
@@ -102,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sm.full[s]), 1);
-      mbar_init(smem_u32(&sm.empty[s]), kRows);
+      mbar_init(smem_u32(&sm.empty[s]), kCompute);
     }
     sm.abort = 0;
     fence_mbar_init();
@@ -110,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   WaitCtx wctx{err, &sm.abort, timeout_ns};
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
       prefetch_tmap(&tm_k_in);
@@ -138,7 +143,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   } else {
     // ----------------------------------------------------------- compute
-    const uint32_t r = static_cast<uint32_t>(tid);  // row within tile
+    // Threads 2r and 2r + 1 share row r.  With H128 = [[H64, H64], [H64, -H64]]
+    // (Sylvester order), half h of (x H128) is H64 applied to x_lo + x_hi
+    // (h = 0) or x_lo - x_hi (h = 1): each thread reads the whole row, forms
+    // its 64 sums or differences and runs a 64-point FWHT in registers.
+    const uint32_t r = static_cast<uint32_t>(tid) >> 1;  // row within tile
+    const int h = tid & 1;
+    const float sg = h ? -1.f : 1.f;
     int it = 0;
     for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
       const int s = it % kStages;
@@ -148,41 +159,43 @@ __global__ void __launch_bounds__(kThreads, 2)
       // for the stage's release runs out)
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.full[s]), ph, wctx))) break;
 
-      // read my row: element e at chunk e/64, granule (e%64)/8, swizzled
-      float x[128];
+      // x[i] = row[i] +- row[i + 64]; element e of the row sits in 64-column
+      // chunk e/64, granule (e%64)/8, swizzled
+      float x[64];
       const uint8_t *tile = sm.in[s];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int g = 0; g < 8; ++g) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(tile + sw128_off(r, g));
+        const uint4 b = *reinterpret_cast<const uint4 *>(tile + kInTileBytes / 2 + sw128_off(r, g));
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const uint4 v = *reinterpret_cast<const uint4 *>(tile + c * (kInTileBytes / 2) + sw128_off(r, g));
-          const int e = c * 64 + g * 8;
-          x[e + 0] = bf16lo_to_f32(v.x);
-          x[e + 1] = bf16hi_to_f32(v.x);
-          x[e + 2] = bf16lo_to_f32(v.y);
-          x[e + 3] = bf16hi_to_f32(v.y);
-          x[e + 4] = bf16lo_to_f32(v.z);
-          x[e + 5] = bf16hi_to_f32(v.z);
-          x[e + 6] = bf16lo_to_f32(v.w);
-          x[e + 7] = bf16hi_to_f32(v.w);
+        for (int k = 0; k < 4; ++k) {
+          const float2 lo = make_float2(bf16lo_to_f32(aw[k]), bf16hi_to_f32(aw[k]));
+          const float2 hi = make_float2(bf16lo_to_f32(bw[k]), bf16hi_to_f32(bw[k]));
+          const float2 u = __ffma2_rn(hi, make_float2(sg, sg), lo);
+          x[g * 8 + 2 * k] = u.x;
+          x[g * 8 + 2 * k + 1] = u.y;
         }
       }
       mbar_arrive(smem_u32(&sm.empty[s]));
 
-      fwht128_packed(x);  // x now holds sqrt(128) * (row H)
+      fwht64_packed(x);  // x now holds sqrt(128) * (row H), elements 64h .. 64h + 63
 
-      RowScale rs[kGroups];
+      constexpr int kMine = kGroups == 1 ? 1 : kGroups / 2;  // scale groups within this half
+      RowScale rs[kMine];
       if constexpr (kGroups == 1) {
         float am[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int e = 0; e < 128; e += 8) {
+        for (int e = 0; e < 64; e += 8) {
 #pragma unroll
           for (int u = 0; u < 4; ++u) am[u] = fmax3(am[u], fabsf(x[e + 2 * u]), fabsf(x[e + 2 * u + 1]));
         }
-        rs[0] = row_scale(fmax3(am[0], am[1], fmaxf(am[2], am[3])));
+        float a = fmax3(am[0], am[1], fmaxf(am[2], am[3]));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        rs[0] = row_scale(a);
       } else {
 #pragma unroll
-        for (int gi = 0; gi < kGroups; ++gi) {
+        for (int gi = 0; gi < kMine; ++gi) {
           constexpr int kW = 128 / kGroups;
           float am[2] = {0.f, 0.f};
 #pragma unroll
@@ -201,16 +214,16 @@ __global__ void __launch_bounds__(kThreads, 2)
       const bool is_v = t >= tiles_per_tensor;
       const int64_t row0 = (is_v ? t - tiles_per_tensor : t) * kRows;
       const bool row_ok = row0 + r < rows;
-      int8_t *oc = (is_v ? v_codes : k_codes) + (row_ok ? row0 + r : 0) * 128;
+      int8_t *oc = (is_v ? v_codes : k_codes) + (row_ok ? row0 + r : 0) * 128 + 64 * h;
       uint32_t wp[8];  // granules g - 1 and g, stored together when kWide
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
+      for (int g = 0; g < 4; ++g) {
         uint32_t w[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           uint32_t q[4];
           const int e = g * 16 + k * 4;
-          const RowScale &gs = rs[(e * kGroups) >> 7];
+          const RowScale &gs = rs[kGroups == 1 ? 0 : (e * kGroups) >> 7];
           const float m = gs.m;
           if (!gs.clamp) {
             const float2 mm = make_float2(m, m), mg = make_float2(kMagic, kMagic);
@@ -239,8 +252,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       uint16_t *scales = is_v ? v_scales : k_scales;
       if (row_ok) {
+        if constexpr (kGroups == 1) {
+          if (h == 0) scales[row0 + r] = __half_as_ushort(rs[0].sh);
+        } else {
 #pragma unroll
-        for (int gi = 0; gi < kGroups; ++gi) scales[(row0 + r) * kGroups + gi] = __half_as_ushort(rs[gi].sh);
+          for (int gi = 0; gi < kMine; ++gi)
+            scales[(row0 + r) * kGroups + kMine * h + gi] = __half_as_ushort(rs[gi].sh);
+        }
       }
     }
   }
