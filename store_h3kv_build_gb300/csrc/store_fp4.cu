@@ -8,19 +8,22 @@
 // GB300 design: the HBM-bound stream of the kvi8r build.  A persistent grid
 // (two CTAs per SM) walks 128-row tiles (K tiles, then V tiles); one producer
 // warp streams bf16 tiles into a 3-stage ring with TMA (128-byte swizzle), and
-// four compute warps own one row per thread and store its 64 code bytes (two
-// 32-byte stores when the code buffers are 32-byte aligned, else four
-// 16-byte ones) and 8 scale bytes straight from registers.
+// eight compute warps give every row two threads, one per 64-value half (four
+// 16-value blocks).  Each thread stores its half row's 32 code bytes (one
+// 32-byte store when the code buffers are 32-byte aligned, else two 16-byte
+// ones) and 4 scale bytes straight from registers.
 #include "kernels.h"
 #include "ptx.cuh"
 
 namespace h3kv {
 namespace {
 
-constexpr int kRows = 128;                  // rows per tile = compute threads
+constexpr int kRows = 128;                  // rows per tile
+constexpr int kCompute = 2 * kRows;         // two compute threads per row
 constexpr int kStages = 3;                  // input ring depth (2 CTAs per SM)
 constexpr int kInTileBytes = kRows * 256;   // bf16 [128 x 128]
-constexpr int kThreads = kRows + 32;        // 4 compute warps + 1 producer warp
+constexpr int kThreads = kCompute + 32;     // 8 compute warps + 1 producer warp
+constexpr int kProducerWarp = kCompute / 32;
 
 struct Fp4BuildSmem {
   uint8_t in[kStages][kInTileBytes];
@@ -82,7 +85,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sm.full[s]), 1);
-      mbar_init(smem_u32(&sm.empty[s]), kRows);
+      mbar_init(smem_u32(&sm.empty[s]), kCompute);
     }
     sm.abort = 0;
     fence_mbar_init();
@@ -90,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   WaitCtx wctx{err, &sm.abort, timeout_ns};
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
       prefetch_tmap(&tm_k_in);
@@ -117,7 +120,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   } else {
     // ----------------------------------------------------------- compute
-    const uint32_t r = static_cast<uint32_t>(tid);  // row within tile
+    // Threads 2r and 2r + 1 share row r: thread h takes values 64h .. 64h + 63
+    // (blocks 4h .. 4h + 3).  For K, H128 = [[H64, H64], [H64, -H64]], so
+    // half h of the rotated row is H64 applied to x_lo + x_hi (h = 0) or
+    // x_lo - x_hi (h = 1); V is taken as it is.
+    const uint32_t r = static_cast<uint32_t>(tid) >> 1;  // row within tile
+    const int h = tid & 1;
+    const float sg = h ? -1.f : 1.f;
     int it = 0;
     for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
       const int s = it % kStages;
@@ -127,33 +136,46 @@ __global__ void __launch_bounds__(kThreads, 2)
       // for the stage's release runs out)
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.full[s]), ph, wctx))) break;
 
-      float x[128];
+      const bool is_v = t >= tiles_per_tensor;
+      float x[64];
       const uint8_t *tile = sm.in[s];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      if (!is_v) {
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
-          const uint4 v = *reinterpret_cast<const uint4 *>(tile + c * (kInTileBytes / 2) + sw128_off(r, g));
-          const int e = c * 64 + g * 8;
-          x[e + 0] = bf16lo_to_f32(v.x);
-          x[e + 1] = bf16hi_to_f32(v.x);
-          x[e + 2] = bf16lo_to_f32(v.y);
-          x[e + 3] = bf16hi_to_f32(v.y);
-          x[e + 4] = bf16lo_to_f32(v.z);
-          x[e + 5] = bf16hi_to_f32(v.z);
-          x[e + 6] = bf16lo_to_f32(v.w);
-          x[e + 7] = bf16hi_to_f32(v.w);
+          const uint4 a = *reinterpret_cast<const uint4 *>(tile + sw128_off(r, g));
+          const uint4 b = *reinterpret_cast<const uint4 *>(tile + kInTileBytes / 2 + sw128_off(r, g));
+          const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 lo = make_float2(bf16lo_to_f32(aw[k]), bf16hi_to_f32(aw[k]));
+            const float2 hi = make_float2(bf16lo_to_f32(bw[k]), bf16hi_to_f32(bw[k]));
+            const float2 u = __ffma2_rn(hi, make_float2(sg, sg), lo);
+            x[g * 8 + 2 * k] = u.x;
+            x[g * 8 + 2 * k + 1] = u.y;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(tile + h * (kInTileBytes / 2) + sw128_off(r, g));
+          x[g * 8 + 0] = bf16lo_to_f32(v.x);
+          x[g * 8 + 1] = bf16hi_to_f32(v.x);
+          x[g * 8 + 2] = bf16lo_to_f32(v.y);
+          x[g * 8 + 3] = bf16hi_to_f32(v.y);
+          x[g * 8 + 4] = bf16lo_to_f32(v.z);
+          x[g * 8 + 5] = bf16hi_to_f32(v.z);
+          x[g * 8 + 6] = bf16lo_to_f32(v.w);
+          x[g * 8 + 7] = bf16hi_to_f32(v.w);
         }
       }
       mbar_arrive(smem_u32(&sm.empty[s]));
 
-      const bool is_v = t >= tiles_per_tensor;
       if (!is_v) {
         // k' = k H: the unnormalised transform, then 2^-3.5
-        fwht128_packed(x);
+        fwht64_packed(x);
         const float2 inv = make_float2(kInvSqrt128, kInvSqrt128);
 #pragma unroll
-        for (int e = 0; e < 128; e += 2) {
+        for (int e = 0; e < 64; e += 2) {
           const float2 p = __fmul2_rn(make_float2(x[e], x[e + 1]), inv);
           x[e] = p.x;
           x[e + 1] = p.y;
@@ -162,12 +184,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 
       const int64_t row0 = (is_v ? t - tiles_per_tensor : t) * kRows;
       const bool row_ok = row0 + r < rows;
-      uint8_t *oc = (is_v ? v_codes : k_codes) + (row_ok ? row0 + r : 0) * 64;
-      uint32_t sw[2] = {0u, 0u};
-      uint32_t wp[8];  // chunks c - 1 and c, stored together when kWide
+      uint8_t *oc = (is_v ? v_codes : k_codes) + (row_ok ? row0 + r : 0) * 64 + 32 * h;
+      uint32_t sw = 0u;
+      uint32_t wp[8];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        // blocks 2c and 2c + 1 fill 16-byte chunk c of the row's 64 code bytes
+      for (int c = 0; c < 2; ++c) {
+        // local blocks 2c and 2c + 1 fill 16-byte chunk c of this half's 32 code bytes
         uint2 w[2];
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
@@ -182,22 +204,25 @@ __global__ void __launch_bounds__(kThreads, 2)
           constexpr float kRcp6 = 0.16666667163372040f;  // 1/6 rounded to fp32
           const uint32_t sb = f32_to_e4m3(div_step(fmaxf(am[0], am[1]), 6.0f, kRcp6));
           const float sf = __half2float(__ushort_as_half(static_cast<uint16_t>(e4m3_to_f16x2_dup(sb))));
-          sw[blk >> 2] |= sb << ((blk & 3) * 8);
+          sw |= sb << (blk * 8);
           w[hb] = encode_block(xb, sf, sf > 0.f ? rcp_approx(sf) : 0.f);
           if (!(sf > 0.f)) w[hb] = make_uint2(0u, 0u);
         }
-        if constexpr (kWide) {
-          wp[(c & 1) * 4 + 0] = w[0].x;
-          wp[(c & 1) * 4 + 1] = w[0].y;
-          wp[(c & 1) * 4 + 2] = w[1].x;
-          wp[(c & 1) * 4 + 3] = w[1].y;
-          if ((c & 1) && row_ok) st_global_v8(oc + (c - 1) * 16, wp);
-        } else {
-          if (row_ok) *reinterpret_cast<uint4 *>(oc + c * 16) = make_uint4(w[0].x, w[0].y, w[1].x, w[1].y);
-        }
+        wp[c * 4 + 0] = w[0].x;
+        wp[c * 4 + 1] = w[0].y;
+        wp[c * 4 + 2] = w[1].x;
+        wp[c * 4 + 3] = w[1].y;
       }
-      uint8_t *scales = is_v ? v_scales : k_scales;
-      if (row_ok) *reinterpret_cast<uint2 *>(scales + (row0 + r) * 8) = make_uint2(sw[0], sw[1]);
+      if (row_ok) {
+        if constexpr (kWide) {
+          st_global_v8(oc, wp);
+        } else {
+          *reinterpret_cast<uint4 *>(oc) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
+          *reinterpret_cast<uint4 *>(oc + 16) = make_uint4(wp[4], wp[5], wp[6], wp[7]);
+        }
+        uint8_t *scales = is_v ? v_scales : k_scales;
+        *reinterpret_cast<uint32_t *>(scales + (row0 + r) * 8 + 4 * h) = sw;
+      }
     }
   }
   __syncthreads();
