@@ -41,7 +41,8 @@ HEAD_DIM = 128
 MUFU_EX2_PER_CLK_PER_SM = 32  # ex2 throughput measured on GB300 (a dependent-free MUFU loop)
 KERNEL_SOURCES = ["store_h3kv_build_gb300/csrc/attend.cuh", "store_h3kv_build_gb300/csrc/attend_kvi8r.cu",
                   "store_h3kv_build_gb300/csrc/ptx.cuh"]
-BUILD_SOURCES = ["store_h3kv_build_gb300/csrc/store_build.cu", "store_h3kv_build_gb300/csrc/ptx.cuh"]
+BUILD_SOURCES = ["store_h3kv_build_gb300/csrc/store_build.cu", "store_h3kv_build_gb300/csrc/ptx.cuh",
+                 "store_h3kv_build_gb300/csrc/store_fwht.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attend_kvi8r_traffic_h32_l217088.md")
 BUILD_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "store_build_traffic_h4_l217088.md")
 

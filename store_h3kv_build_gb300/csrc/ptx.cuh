@@ -526,33 +526,6 @@ __device__ __forceinline__ float bf16hi_to_f32(uint32_t w) { return __uint_as_fl
 // two at a time in packed fp32 (a + b with one add, a - b as fma(b, -1, a),
 // both exactly rounded, so every value is the scalar transform's bit for
 // bit).
-// Unnormalised 64-point FWHT (Sylvester order) of x in place, as fwht128_packed.
-__device__ __forceinline__ void fwht64_packed(float (&x)[64]) {
-#pragma unroll
-  for (int i = 0; i < 64; i += 2) {
-    const float a = x[i], b = x[i + 1];
-    x[i] = a + b;
-    x[i + 1] = a - b;
-  }
-  const float2 neg1 = make_float2(-1.f, -1.f);
-#pragma unroll
-  for (int h = 2; h < 64; h <<= 1) {
-#pragma unroll
-    for (int i = 0; i < 64; i += 2) {
-      if ((i & h) == 0) {
-        const float2 a = make_float2(x[i], x[i + 1]);
-        const float2 b = make_float2(x[i + h], x[i + h + 1]);
-        const float2 sum = __fadd2_rn(a, b);
-        const float2 dif = __ffma2_rn(b, neg1, a);
-        x[i] = sum.x;
-        x[i + 1] = sum.y;
-        x[i + h] = dif.x;
-        x[i + h + 1] = dif.y;
-      }
-    }
-  }
-}
-
 __device__ __forceinline__ void fwht128_packed(float (&x)[128]) {
 #pragma unroll
   for (int i = 0; i < 128; i += 2) {

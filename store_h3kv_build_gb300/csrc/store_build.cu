@@ -17,6 +17,7 @@
 // shares its absmax with one shuffle.
 #include "kernels.h"
 #include "ptx.cuh"
+#include "store_fwht.cuh"
 
 namespace h3kv {
 namespace {

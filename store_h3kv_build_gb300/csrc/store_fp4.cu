@@ -14,6 +14,7 @@
 // ones) and 4 scale bytes straight from registers.
 #include "kernels.h"
 #include "ptx.cuh"
+#include "store_fwht.cuh"
 
 namespace h3kv {
 namespace {
