@@ -233,8 +233,10 @@ h3kv_status h3kv_attend_staged_static(const uint16_t *Q, int64_t q_seq, const h3
  *      row by the same amount, so attention does not need it; it is stored
  *      for inspection.
  *   V: not rotated; per (head, channel) s_v = max over all tokens |v| / 448;
- *      codes e4m3(v / s_v), the exact quotient rounded once (bit-exact),
- *      stored channel-major (V transposed) with a row stride of
+ *      codes e4m3(v / s_v), the exact quotient rounded once (bit-exact
+ *      for every channel whose absmax is at least 2^-100; below that the
+ *      fp32 arithmetic can miss by one step), stored channel-major
+ *      (V transposed) with a row stride of
  *      h3kv_f8_v_stride(seq) bytes; bytes of a row past seq are 0.
  *   The K (and query) codes are the same rounding of quotients of values
  *   that the kernels compute in fp32, formed as x * fp32(1/s).
