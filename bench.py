@@ -194,22 +194,27 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def time_oracle_sample(w, rows=512, head=0, seed=0):
+def time_oracle_sample(w, rows=512, head=0, seed=0, reps=1):
     """The fp64 oracle on a bounded sample of the workload: build the store of
-    one head (all `seq` tokens of K and V) and attend `rows` query rows of that
-    head over it.  Returns (attention TFLOP/s, store GB/s, seconds, desc)."""
+    one head (all `seq` tokens of K and V), then attend `reps` independent
+    sets of `rows` query rows of that head over it, one call each (the
+    oracle holds a call's whole score matrix, so the sample grows by calls,
+    not by rows per call).  Returns (attention TFLOP/s, store GB/s, seconds,
+    desc)."""
     import oracle
-    q = synth.normal_bf16((1, rows, HEAD_DIM), seed + 100)
+    qs = [synth.normal_bf16((1, rows, HEAD_DIM), seed + 100 + 7 * i) for i in range(reps)]
     k = synth.make_k(1, w["seq"], seed + 101, w["k_outliers"])
     v = synth.normal_bf16((1, w["seq"], HEAD_DIM), seed + 102)
     t0 = time.perf_counter()
     st = oracle.build_store(k, v)
     t1 = time.perf_counter()
-    oracle.attend(q, st)
+    for q in qs:
+        oracle.attend(q, st)
     t2 = time.perf_counter()
-    att = attention_flops(1, rows, w["seq"]) / (t2 - t1) / 1e12
+    att = attention_flops(1, rows * reps, w["seq"]) / (t2 - t1) / 1e12
     gbs = store_bytes(1, w["seq"]) / (t1 - t0) / 1e9
-    desc = (f"oracle (NumPy fp64): store of 1 head x {w['seq']} tokens, then {rows} query rows of that head "
+    sets = f"{reps} x {rows}" if reps > 1 else f"{rows}"
+    desc = (f"oracle (NumPy fp64): store of 1 head x {w['seq']} tokens, then {sets} query rows of that head "
             f"attended over all {w['seq']} keys")
     return att, gbs, t2 - t0, desc
 
@@ -623,10 +628,10 @@ def run_ours(args, w, name):
             "clocks": clocks.summary(),
         }
         if not args.no_cpu_baseline:
-            att, gbs, s, desc = time_oracle_sample(w, rows=args.ref_rows)
+            att, gbs, s, desc = time_oracle_sample(w, rows=args.ref_rows, reps=args.ref_reps)
             line["cpu_baseline"] = {"value": att, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-                                    "sample": f"1 head x {L} tokens: store, then {args.ref_rows} query rows "
-                                              "over all keys (NumPy fp64)",
+                                    "sample": f"1 head x {L} tokens: store, then {args.ref_reps} x {args.ref_rows} "
+                                              "query rows over all keys (NumPy fp64)",
                                     "store_gbs": gbs, "seconds": s}
             detail["cpu_baseline"] = {"sample": desc, "os_cpu_count": os.cpu_count(),
                                       "full_call_s_extrapolated": flops / (att * 1e12) + store_bytes(H, L) / (gbs * 1e9),
@@ -657,7 +662,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="h32_l217088_outlier", choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--ref-rows", type=int, default=2048, help="query rows in the oracle's bounded sample")
+    ap.add_argument("--ref-rows", type=int, default=2048, help="query rows per oracle call in its bounded sample")
+    ap.add_argument("--ref-reps", type=int, default=4,
+                    help="oracle calls in the cpu_baseline sample (about 10-15 s of CPU work at the default)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="omit the oracle timing (used for profiler runs only)")
     ap.add_argument("--only", default="all",
