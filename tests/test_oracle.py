@@ -364,3 +364,28 @@ def test_grouped_attention_closer_to_exact():
     r_row = oracle.rel_rms(oracle.attend(Q, oracle.build_store(K, V)), ex)
     r_grp = oracle.rel_rms(oracle.attend(Q, oracle.build_store_grouped(K, V)), ex)
     assert r_grp < r_row
+
+
+# ------------------------------------------------------------------ rel_rms --
+def test_rel_rms_closed_forms():
+    # rel_rms is the kind of relative error the kv_store row quotes for the
+    # lower store rungs; pinned by values fixed without its formula
+    b = oracle.as_f64(bf16_normal((3, 40, 128), 80))
+    assert oracle.rel_rms(b, b) == 0.0
+    assert oracle.rel_rms(np.zeros_like(b), b) == pytest.approx(1.0, rel=1e-15)
+    # a uniform relative error eps gives exactly |eps|, of either sign
+    for eps in (1e-3, -0.25, 2.0):
+        assert oracle.rel_rms(b * (1 + eps), b) == pytest.approx(abs(eps), rel=1e-12)
+    # joint scaling leaves it unchanged; it is not symmetric in its arguments
+    a = b + oracle.as_f64(bf16_normal((3, 40, 128), 81)) * 0.1
+    assert oracle.rel_rms(7.5 * a, 7.5 * b) == pytest.approx(oracle.rel_rms(a, b), rel=1e-12)
+    assert oracle.rel_rms(2 * b, b) == pytest.approx(1.0) and oracle.rel_rms(b, 2 * b) == pytest.approx(0.5)
+
+
+def test_rel_rms_hand_worked():
+    # a = (1, 2), b = (1, 1): the difference is (0, 1), so the error's norm is
+    # 1 against the reference's sqrt(2): 1/sqrt(2)
+    assert oracle.rel_rms(np.array([1.0, 2.0]), np.array([1.0, 1.0])) == pytest.approx(2 ** -0.5, rel=1e-15)
+    # a = (3, 0, 4), b = (0, 0, 5): difference (3, 0, -1), norm sqrt(10) against 5
+    assert oracle.rel_rms(np.array([3.0, 0.0, 4.0]), np.array([0.0, 0.0, 5.0])) == pytest.approx(10 ** 0.5 / 5,
+                                                                                                   rel=1e-15)
