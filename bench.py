@@ -87,6 +87,16 @@ def workload_desc(name, w):
     }
 
 
+def line_config(name, w):
+    """The `config` object of the JSON line, the same for both arms."""
+    kv_bytes = 2 * w["heads"] * w["seq"] * HEAD_DIM * 2
+    l2 = ("no flush: inputs far larger than L2" if kv_bytes > 4 * 129e6 else
+          "no flush: inputs larger than L2" if kv_bytes > 129e6 else
+          "no flush: inputs fit in L2 (a parity configuration, not the bench workload)")
+    return {"workload": name, "heads": w["heads"], "seq": w["seq"], "head_dim": HEAD_DIM, "q_chunk": w["q_chunk"],
+            "kv_block": w["kv_block"], "k_outliers": w["k_outliers"], "l2": l2}
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -304,7 +314,8 @@ def run_reference(args, w, name):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(secs),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_desc(name, w),
+        "config": line_config(name, w),
+        "workload_desc": workload_desc(name, w)["workload"],
         "store_build": {"value": statistics.median(gbs_all), "unit": "GB/s"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -601,9 +612,7 @@ def run_ours(args, w, name):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
-            "config": {"workload": name, "heads": H, "seq": L, "head_dim": HEAD_DIM, "q_chunk": q_chunk,
-                       "kv_block": kv_block, "k_outliers": w["k_outliers"],
-                       "l2": "no flush: inputs far larger than L2"},
+            "config": line_config(name, w),
             "roofline": {"bound": "tensor", "kernel": "attend_kernel<kvi8r>", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "frac_of_burst": achieved / peaks["bf16_tflops"],
                          "peak_source": f"{peak_src} bf16 sustained", "traffic": traffic,
