@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define H3KV_ABI_VERSION 6u
+#define H3KV_ABI_VERSION 7u
 #define H3KV_HEAD_DIM 128
 /* kv_block = 0 on the kvi8r path means this many tokens (the kv_block
  * default of the kv_store row). */
@@ -358,6 +358,16 @@ h3kv_status h3kv_debug_withhold_p(int32_t tile);
  * H3KV_ERR_DEVICE_TIMEOUT in the device error word and returns, so the next
  * h3kv_sync_status() on `stream` reports it.  Nothing faults or traps. */
 h3kv_status h3kv_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
+
+/* Diagnostic of the reducing tensor-memory load (tcgen05.ld.red, sm_103a)
+ * with which every attention path takes the row maximum of a full 128-key
+ * tile: one CTA stores known fp32 values into 128 TMEM columns of each of its
+ * 128 lanes, reloads them with the max reduction over each 32-column group,
+ * and counts the reduced maxima that differ from the maxima of the stored
+ * values plus the loaded values that differ from the stored ones.  Writes
+ * the count to *mismatches (0 when the instruction behaves as the kernels
+ * assume); synchronises `stream`.  NULL mismatches: H3KV_ERR_INVALID_ARG. */
+h3kv_status h3kv_selftest_tmem_ld_max(int32_t *mismatches, void *stream);
 
 /* Static description of a status code (never NULL). */
 const char *h3kv_strerror(h3kv_status status);

@@ -94,6 +94,7 @@ _SIGS = {
     "h3kv_attend_fp4": (ctypes.c_int, [_vp, _i64, ctypes.POINTER(h3kv_store_fp4), _i32, _i32, _f32, _vp, _vp]),
     "h3kv_set_wait_timeout_ns": (ctypes.c_int, [ctypes.c_uint64]),
     "h3kv_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _vp]),
+    "h3kv_selftest_tmem_ld_max": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), _vp]),
     "h3kv_debug_withhold_p": (ctypes.c_int, [ctypes.c_int32]),
     "h3kv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
 }

@@ -39,6 +39,53 @@ __global__ void wait_selftest_kernel(uint32_t *err, uint64_t timeout_ns) {
   __syncthreads();
 }
 
+// Checks the reducing TMEM load of the attention kernels (tmem_ld128_max):
+// one CTA of 128 threads allocates 128 TMEM columns, each thread stores
+// known fp32 values (both signs, the group maxima at row-dependent columns)
+// into the 128 columns of its lane, reloads them, and counts each 32-column
+// group whose reduced maximum differs from the maximum of what it stored,
+// and each loaded value that differs from the stored one.
+__device__ int32_t g_tmem_selftest_mismatches;
+__global__ void tmem_ld_max_selftest_kernel() {
+  __shared__ uint32_t slot;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (warp == 0) {
+    h3kv::tmem_alloc(h3kv::smem_u32(&slot), 128);
+    h3kv::tmem_relinquish();
+  }
+  h3kv::tc_fence_before();
+  __syncthreads();
+  h3kv::tc_fence_after();
+  const uint32_t taddr = slot + (static_cast<uint32_t>(warp * 32) << 16);
+  uint32_t v[128];
+  float want[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int c = 0; c < 128; ++c) {
+    float x = static_cast<float>(((tid * 37 + c * 101) % 257) - 128) * 0.37f;
+    if ((c & 31) == (tid * 7 + (c >> 5)) % 32) x = 50.0f + 0.25f * tid + (c >> 5);
+    v[c] = __float_as_uint(x);
+    want[c >> 5] = fmaxf(want[c >> 5], x);
+  }
+#pragma unroll
+  for (int g = 0; g < 4; ++g) h3kv::tmem_st32(taddr + 32 * g, *reinterpret_cast<const uint32_t(*)[32]>(v + 32 * g));
+  h3kv::tmem_wait_st();
+  uint32_t r[128];
+  float m[4];
+  h3kv::tmem_ld128_max(taddr, r, m);
+  int bad = 0;
+#pragma unroll
+  for (int c = 0; c < 128; ++c) bad += r[c] != v[c];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) bad += m[g] != want[g];
+  if (bad) atomicAdd(&g_tmem_selftest_mismatches, bad);
+  h3kv::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    h3kv::tc_fence_after();
+    h3kv::tmem_dealloc(slot, 128);
+  }
+}
+
 struct DeviceInfo {
   bool ready = false;
   bool supported = false;
@@ -772,6 +819,25 @@ h3kv_status h3kv_selftest_wait_timeout(uint64_t timeout_ns, void *stream) {
   wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
       d->err, timeout_ns == 0 ? kDefaultTimeoutNs : timeout_ns);
   return cudaGetLastError() == cudaSuccess ? H3KV_OK : H3KV_ERR_CUDA;
+}
+
+h3kv_status h3kv_selftest_tmem_ld_max(int32_t *mismatches, void *stream) {
+  if (!mismatches) return H3KV_ERR_INVALID_ARG;
+  DeviceInfo *d = nullptr;
+  h3kv_status st = device_info(&d);
+  if (st != H3KV_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int32_t zero = 0;
+  if (cudaMemcpyToSymbolAsync(g_tmem_selftest_mismatches, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s) !=
+      cudaSuccess)
+    return H3KV_ERR_CUDA;
+  tmem_ld_max_selftest_kernel<<<1, 128, 0, s>>>();
+  if (cudaGetLastError() != cudaSuccess) return H3KV_ERR_CUDA;
+  if (cudaMemcpyFromSymbolAsync(mismatches, g_tmem_selftest_mismatches, sizeof(int32_t), 0, cudaMemcpyDeviceToHost,
+                                s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return H3KV_ERR_CUDA;
+  return H3KV_OK;
 }
 
 h3kv_status h3kv_sync_status(void *stream) {

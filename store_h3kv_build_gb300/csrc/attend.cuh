@@ -383,14 +383,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       float s[128];
-      tmem_ld128(tS, *reinterpret_cast<uint32_t(*)[128]>(s));
       const int64_t valid = a.kv_seq - static_cast<int64_t>(j) * kBN;
-      if (valid < kBN) {
+      // The row max of a full tile comes with the S loads (the reducing
+      // TMEM load returns each 32-column group's maximum: 3.5 % faster on
+      // kvi8r, outputs bit-identical); the tile past the last key masks its
+      // columns beyond `valid` and takes the max in software.  The two
+      // arrangements of the loads below are the ones that compile without
+      // spills for the quantised and the exact stores.
+      float mt;
+      float m4[4];
+      if constexpr (kKvi8r) tmem_ld128_max(tS, *reinterpret_cast<uint32_t(*)[128]>(s), m4);
+      if (valid >= kBN) {
+        if constexpr (!kKvi8r) tmem_ld128_max(tS, *reinterpret_cast<uint32_t(*)[128]>(s), m4);
+        mt = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+      } else {
+        if constexpr (!kKvi8r) tmem_ld128(tS, *reinterpret_cast<uint32_t(*)[128]>(s));
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = (c < valid) ? s[c] : -INFINITY;
-      }
-      float mt;
-      {
         // eight independent chains of 16 columns (0.3 % faster than four)
         float m8[8];
 #pragma unroll

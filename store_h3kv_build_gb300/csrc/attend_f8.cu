@@ -176,7 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       float s[128];
-      tmem_ld128(tS, *reinterpret_cast<uint32_t(*)[128]>(s));
+      float m4[4];  // raw maxima of the four 32-key groups, from the loads
+      tmem_ld128_max(tS, *reinterpret_cast<uint32_t(*)[128]>(s), m4);
       float mult0 = cq * sk0, mult1 = cq * sk1;
       const int64_t valid = a.kv_seq - static_cast<int64_t>(j) * kBN;
       if (valid < kBN) {
@@ -186,8 +187,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mult0 = mult1 = 1.f;
       }
       float mt;
-      {
+      if (valid >= kBN) {
         // raw maxima of each 64-key half, then scaled (multipliers >= 0)
+        mt = fmaxf(fmaxf(m4[0], m4[1]) * mult0, fmaxf(m4[2], m4[3]) * mult1);
+      } else {
+        // the tail tile, scaled and masked above
         // elements 2 .. 63 of each half: 31 pairs over two accumulators
         float h0[2] = {s[0], s[1]}, h1[2] = {s[64], s[65]};
 #pragma unroll

@@ -21,7 +21,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported():
     names = declared_functions()
-    assert len(names) == 22
+    assert len(names) == 23
     assert {"h3kv_attend_f8", "h3kv_build_store_f8", "h3kv_f8_v_stride", "h3kv_store_f8_bytes"} <= set(names)
     assert {"h3kv_attend_fp4", "h3kv_build_store_fp4", "h3kv_store_fp4_bytes"} <= set(names)
     lib = ctypes.CDLL(b.LIB_PATH)
@@ -31,7 +31,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_abi_version_and_strings():
-    assert b.h3kv_abi_version() == 6
+    assert b.h3kv_abi_version() == 7
     for st in range(5):
         assert b.h3kv_strerror(st)
     assert b.h3kv_strerror(99) == b"unknown status"
@@ -244,3 +244,8 @@ def test_attention_rejects_more_than_65535_heads():
     assert b.h3kv_attend_fp4(4096, 16, ctypes.byref(st4), 16, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
     st8 = b.h3kv_store_f8(4096, 4096, 4096, 4096, 4096, H, 16, 128)
     assert b.h3kv_attend_f8(4096, 16, ctypes.byref(st8), 16, 0, 0.0, 4096, None) == b.H3KV_ERR_INVALID_ARG
+
+
+def test_tmem_selftest_rejects_null_before_device_work():
+    # the argument check comes before the device query, so no GPU is needed
+    assert b.h3kv_selftest_tmem_ld_max(None, None) == b.H3KV_ERR_INVALID_ARG
