@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int h = blockIdx.y;
+  const int h = a.head_base + static_cast<int>(blockIdx.y);
   const int64_t row0 = a.q_begin + static_cast<int64_t>(blockIdx.x) * (kNQ * kBM);
   const int n_tiles = static_cast<int>((a.kv_seq + kBN - 1) / kBN);
   const int blk = a.kv_block_tiles;

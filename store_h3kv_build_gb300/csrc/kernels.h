@@ -51,7 +51,8 @@ struct AttnArgs {
   int64_t kv_stride;        // rows between heads in the K/V store arrays (kv_seq unless staged)
   int64_t q_begin;          // this launch's query chunk [q_begin, q_end)
   int64_t q_end;
-  int32_t heads;
+  int32_t heads;            // heads of this launch (grid rows)
+  int32_t head_base;        // the head of grid row 0
   int32_t kv_block_tiles;   // 128-key tiles per kv_block
   float scale_log2;         // softmax_scale * log2(e)
   uint32_t *err;
@@ -77,14 +78,16 @@ struct AttnArgs {
 
 constexpr int kAttnRowsPerCta = 256;  // two 128-row query tiles per CTA
 
-// One launch over the query chunk [args.q_begin, args.q_end) of every head.
+// One launch over the query chunk [args.q_begin, args.q_end) of heads
+// args.head_base .. args.head_base + args.heads - 1 (one grid row each).
 // The exact path reads Q, K, V through 3-D tensor maps ({128, seq, heads},
 // box 64 x 128 x 1, 128B swizzle); the kvi8r path reads Q with plain loads
 // and the store with bulk copies (the maps are unused).
 // overlap_previous: launch with programmatic stream serialization, so that
 // this grid's CTAs may start on SMs the previous launch's tail frees.  Only
-// for a launch that touches nothing the previous kernel writes (the next
-// query chunk of the same call); the kernels keep completion in stream order.
+// for a launch that touches nothing the previous kernel writes (another
+// query chunk or head of the same call); the kernels keep completion in
+// stream order.
 cudaError_t launch_attend_kvi8r(const AttnArgs &args, bool overlap_previous, cudaStream_t stream);
 
 // kvfp4 store build: K rotated, V not; per 16-value block an e4m3 scale and
@@ -118,7 +121,8 @@ struct F8Args {
   int64_t kv_seq;
   int64_t q_begin;          // this launch's query chunk [q_begin, q_end)
   int64_t q_end;
-  int32_t heads;
+  int32_t heads;            // heads of this launch (grid rows)
+  int32_t head_base;        // the head of grid row 0
   int32_t kv_block_tiles;   // 128-key tiles per kv_block
   int32_t k_blocks;         // ceil(kv_seq / 64)
   float scale_log2;         // softmax_scale * log2(e)
