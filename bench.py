@@ -40,7 +40,7 @@ UNIT = "TFLOP/s"
 HEAD_DIM = 128
 MUFU_EX2_PER_CLK_PER_SM = 32  # ex2 throughput measured on GB300 (a dependent-free MUFU loop)
 KERNEL_SOURCES = ["store_h3kv_build_gb300/csrc/attend.cuh", "store_h3kv_build_gb300/csrc/attend_kvi8r.cu",
-                  "store_h3kv_build_gb300/csrc/ptx.cuh"]
+                  "store_h3kv_build_gb300/csrc/ptx.cuh", "store_h3kv_build_gb300/csrc/launch_order.h"]
 BUILD_SOURCES = ["store_h3kv_build_gb300/csrc/store_build.cu", "store_h3kv_build_gb300/csrc/ptx.cuh",
                  "store_h3kv_build_gb300/csrc/store_fwht.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attend_kvi8r_traffic_h32_l217088.md")
@@ -129,14 +129,15 @@ def read_summary_values(path):
 
 
 def recorded_traffic(heads, seq):
-    """DRAM bytes per full attention launch (16384 query rows x all heads over
-    all keys) from the committed ncu summary, if it was taken on the current
-    kernel source and sequence (else None); scaled by heads if the capture
-    holds fewer heads than the call."""
+    """DRAM bytes of the attention per query chunk of 16384 rows over all
+    heads and keys (the launches of a whole call captured, divided by its
+    chunks) from the committed ncu summary, if it was taken on the current
+    kernel and launch-order sources and sequence (else None); scaled by heads
+    if the capture holds fewer heads than the call."""
     d = read_summary_values(TRAFFIC_FILE)
     if d.get("kernel_src_sha") != kernel_sha() or int(d.get("seq", 0)) != seq:
         return None
-    return float(d["dram_bytes_per_launch"]) * heads / int(d["heads"])
+    return float(d["dram_bytes_per_chunk"]) * heads / int(d["heads"])
 
 
 def recorded_build_traffic(heads, seq):

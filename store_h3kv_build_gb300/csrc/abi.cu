@@ -9,6 +9,7 @@
 #include "../../include/h3kv.h"
 #include "kernels.h"
 #include "ptx.cuh"
+#include "launch_order.h"
 
 namespace {
 
@@ -212,36 +213,6 @@ float scale_log2_of(float softmax_scale) {
   return s * 1.4426950408889634f;
 }
 
-// The launches of one attention call over a device-resident store.  With
-// at least kHeadMajorCtas CTAs per head and query chunk, every query chunk of
-// head 0 is launched, then every chunk of head 1, and so on: the CTAs in
-// flight then read one or two heads' stores, and the L2 keeps much of a
-// head's store for its later chunks (half the DRAM reads of a call in a
-// serialised capture, the same time).  Smaller chunks are launched chunk by
-// chunk over all heads, so that a call never becomes heads x chunks tiny
-// launches.  Every launch after the first follows the one before it with
-// programmatic dependent launch.  A query row's arithmetic is the same in
-// every launch, so results do not depend on the order.
-template <class Args, class Launch>
-h3kv_status launch_query_chunks(Args a, int64_t q_seq, int64_t q_chunk, int32_t heads, Launch launch) {
-  constexpr int64_t kHeadMajorCtas = 16;
-  const int64_t chunk_rows = q_chunk < q_seq ? q_chunk : q_seq;
-  const bool head_major =
-      heads > 1 && (chunk_rows + h3kv::kAttnRowsPerCta - 1) / h3kv::kAttnRowsPerCta >= kHeadMajorCtas;
-  a.heads = head_major ? 1 : heads;
-  bool first = true;
-  for (int32_t hh = 0; hh < (head_major ? heads : 1); ++hh) {
-    a.head_base = hh;
-    for (int64_t c0 = 0; c0 < q_seq; c0 += q_chunk) {
-      a.q_begin = c0;
-      a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
-      if (launch(a, !first) != cudaSuccess) return H3KV_ERR_CUDA;
-      first = false;
-    }
-  }
-  return H3KV_OK;
-}
-
 }  // namespace
 
 extern "C" {
@@ -330,7 +301,7 @@ h3kv_status h3kv_attend(const uint16_t *Q, int64_t q_seq, const h3kv_store *stor
   a.err = d->err;
   a.timeout_ns = g_timeout_ns.load();
   a.withhold_p_tile1 = g_withhold_p_tile1.load();
-  return launch_query_chunks(a, q_seq, q_chunk, store->heads, [&](const h3kv::AttnArgs &x, bool overlap) {
+  return h3kv::launch_query_chunks(a, q_seq, q_chunk, store->heads, [&](const h3kv::AttnArgs &x, bool overlap) {
     return h3kv::launch_attend_kvi8r(x, overlap, static_cast<cudaStream_t>(stream));
   });
 }
@@ -370,7 +341,7 @@ h3kv_status h3kv_attend_exact(const uint16_t *Q, int64_t q_seq, const uint16_t *
   a.err = d->err;
   a.timeout_ns = g_timeout_ns.load();
   a.withhold_p_tile1 = g_withhold_p_tile1.load();
-  return launch_query_chunks(a, q_seq, q_chunk, heads, [&](const h3kv::AttnArgs &x, bool overlap) {
+  return h3kv::launch_query_chunks(a, q_seq, q_chunk, heads, [&](const h3kv::AttnArgs &x, bool overlap) {
     return h3kv::launch_attend_exact(tq, tk, tv, x, overlap, static_cast<cudaStream_t>(stream));
   });
 }
@@ -738,7 +709,7 @@ h3kv_status h3kv_attend_f8(const uint16_t *Q, int64_t q_seq, const h3kv_store_f8
   a.err = d->err;
   a.timeout_ns = g_timeout_ns.load();
   a.withhold_p_tile1 = g_withhold_p_tile1.load();
-  return launch_query_chunks(a, q_seq, q_chunk, store->heads, [&](const h3kv::F8Args &x, bool overlap) {
+  return h3kv::launch_query_chunks(a, q_seq, q_chunk, store->heads, [&](const h3kv::F8Args &x, bool overlap) {
     return h3kv::launch_attend_f8(tk, tv, x, overlap, static_cast<cudaStream_t>(stream));
   });
 }
@@ -810,7 +781,7 @@ h3kv_status h3kv_attend_fp4(const uint16_t *Q, int64_t q_seq, const h3kv_store_f
   a.err = d->err;
   a.timeout_ns = g_timeout_ns.load();
   a.withhold_p_tile1 = g_withhold_p_tile1.load();
-  return launch_query_chunks(a, q_seq, q_chunk, store->heads, [&](const h3kv::AttnArgs &x, bool overlap) {
+  return h3kv::launch_query_chunks(a, q_seq, q_chunk, store->heads, [&](const h3kv::AttnArgs &x, bool overlap) {
     return h3kv::launch_attend_fp4(x, overlap, static_cast<cudaStream_t>(stream));
   });
 }

@@ -1,0 +1,42 @@
+// launch_order.h -- the order in which an attention call over a device-resident
+// store launches its query chunks (and heads).
+#pragma once
+
+#include <stdint.h>
+
+#include "../../include/h3kv.h"
+#include "kernels.h"
+
+namespace h3kv {
+
+// The launches of one attention call over a device-resident store.  With
+// at least kHeadMajorCtas CTAs per head and query chunk, every query chunk of
+// head 0 is launched, then every chunk of head 1, and so on: the CTAs in
+// flight then read one or two heads' stores, and the L2 keeps much of a
+// head's store for its later chunks (half the DRAM reads of a call in a
+// serialised capture, the same time).  Smaller chunks are launched chunk by
+// chunk over all heads, so that a call never becomes heads x chunks tiny
+// launches.  Every launch after the first follows the one before it with
+// programmatic dependent launch.  A query row's arithmetic is the same in
+// every launch, so results do not depend on the order.
+template <class Args, class Launch>
+inline h3kv_status launch_query_chunks(Args a, int64_t q_seq, int64_t q_chunk, int32_t heads, Launch launch) {
+  constexpr int64_t kHeadMajorCtas = 16;
+  const int64_t chunk_rows = q_chunk < q_seq ? q_chunk : q_seq;
+  const bool head_major =
+      heads > 1 && (chunk_rows + kAttnRowsPerCta - 1) / kAttnRowsPerCta >= kHeadMajorCtas;
+  a.heads = head_major ? 1 : heads;
+  bool first = true;
+  for (int32_t hh = 0; hh < (head_major ? heads : 1); ++hh) {
+    a.head_base = hh;
+    for (int64_t c0 = 0; c0 < q_seq; c0 += q_chunk) {
+      a.q_begin = c0;
+      a.q_end = c0 + q_chunk < q_seq ? c0 + q_chunk : q_seq;
+      if (launch(a, !first) != cudaSuccess) return H3KV_ERR_CUDA;
+      first = false;
+    }
+  }
+  return H3KV_OK;
+}
+
+}  // namespace h3kv
