@@ -345,8 +345,8 @@ def run_ours(args, w, name):
     st = b.Store.empty(H, L, dev)
     out = torch.empty((H, L, HEAD_DIM), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    n_chunks = (L + q_chunk - 1) // q_chunk
-    launches_per_step = 1 + n_chunks
+    # the store build, then the call's attention launches (the library's count)
+    launches_per_step = 1 + int(b.h3kv_attend_launch_count(L, H, q_chunk))
 
     def step():
         b.build_store(k, v, out=st)

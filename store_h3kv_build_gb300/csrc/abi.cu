@@ -786,6 +786,10 @@ h3kv_status h3kv_attend_fp4(const uint16_t *Q, int64_t q_seq, const h3kv_store_f
   });
 }
 
+int64_t h3kv_attend_launch_count(int64_t q_seq, int32_t heads, int32_t q_chunk) {
+  return h3kv::launch_count(q_seq, q_chunk, heads);
+}
+
 h3kv_status h3kv_set_wait_timeout_ns(uint64_t timeout_ns) {
   g_timeout_ns.store(timeout_ns == 0 ? kDefaultTimeoutNs : timeout_ns);
   return H3KV_OK;

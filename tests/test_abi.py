@@ -21,7 +21,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported():
     names = declared_functions()
-    assert len(names) == 23
+    assert len(names) == 24
     assert {"h3kv_attend_f8", "h3kv_build_store_f8", "h3kv_f8_v_stride", "h3kv_store_f8_bytes"} <= set(names)
     assert {"h3kv_attend_fp4", "h3kv_build_store_fp4", "h3kv_store_fp4_bytes"} <= set(names)
     lib = ctypes.CDLL(b.LIB_PATH)
@@ -31,7 +31,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_abi_version_and_strings():
-    assert b.h3kv_abi_version() == 7
+    assert b.h3kv_abi_version() == 8
     for st in range(5):
         assert b.h3kv_strerror(st)
     assert b.h3kv_strerror(99) == b"unknown status"
@@ -249,3 +249,18 @@ def test_attention_rejects_more_than_65535_heads():
 def test_tmem_selftest_rejects_null_before_device_work():
     # the argument check comes before the device query, so no GPU is needed
     assert b.h3kv_selftest_tmem_ld_max(None, None) == b.H3KV_ERR_INVALID_ARG
+
+
+def test_attend_launch_count():
+    # one launch per chunk over all heads below 16 CTAs (256 rows each) per head
+    # and chunk, else heads x chunks launches of one head each
+    assert b.h3kv_attend_launch_count(217088, 32, 16384) == 32 * 14
+    assert b.h3kv_attend_launch_count(217088, 32, 4096) == 32 * 53
+    assert b.h3kv_attend_launch_count(217088, 32, 3841) == 32 * 57   # 16 CTAs per chunk
+    assert b.h3kv_attend_launch_count(217088, 32, 3840) == 57        # 15 CTAs per chunk
+    assert b.h3kv_attend_launch_count(65536, 32, 1024) == 64
+    assert b.h3kv_attend_launch_count(3000, 1, 256) == 12        # one head: chunk by chunk
+    assert b.h3kv_attend_launch_count(1000, 8, 16384) == 1        # 4 CTAs per head: one launch
+    assert b.h3kv_attend_launch_count(8192, 8, 16384) == 8        # 32 CTAs per head: per head
+    assert b.h3kv_attend_launch_count(0, 8, 256) == 0
+    assert b.h3kv_attend_launch_count(100, 8, 0) == 0
