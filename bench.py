@@ -346,7 +346,7 @@ def run_ours(args, w, name):
     out = torch.empty((H, L, HEAD_DIM), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     # the store build, then the call's attention launches (the library's count)
-    launches_per_step = 1 + int(b.h3kv_attend_launch_count(L, H, q_chunk))
+    launches_per_step = 1 + int(b.h3kv_attend_launch_count(L, L, H, q_chunk))
 
     def step():
         b.build_store(k, v, out=st)

@@ -360,14 +360,15 @@ h3kv_status h3kv_debug_withhold_p(int32_t tile);
 h3kv_status h3kv_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
 
 /* Kernel launches that one h3kv_attend, h3kv_attend_exact, h3kv_attend_f8 or
- * h3kv_attend_fp4 call makes for `q_seq` query rows of `heads` heads in
- * chunks of `q_chunk` rows (0 for an empty call or a non-positive argument).
- * When a chunk holds at least 16 CTAs of 256 rows (more than 3840 rows) per
- * head and there is more than one head, the call launches every chunk of head 0, then of head 1, and
- * so on (heads x chunks launches, each one head), so that the L2 keeps much
- * of a head's store between its chunks; otherwise one launch per chunk covers
- * all heads.  Results do not depend on the order. */
-int64_t h3kv_attend_launch_count(int64_t q_seq, int32_t heads, int32_t q_chunk);
+ * h3kv_attend_fp4 call makes for `q_seq` query rows of `heads` heads over
+ * `kv_seq` keys in chunks of `q_chunk` rows (0 for an empty call or a
+ * non-positive argument).  With more than one head, at least 131072 keys and
+ * at least 16 CTAs of 256 rows (more than 3840 rows) per head and chunk, the
+ * call launches every chunk of head 0, then of head 1, and so on (heads x
+ * chunks launches, each one head), so that the L2 keeps much of a head's
+ * store between its chunks; otherwise one launch per chunk covers all heads.
+ * Results do not depend on the order. */
+int64_t h3kv_attend_launch_count(int64_t q_seq, int64_t kv_seq, int32_t heads, int32_t q_chunk);
 
 /* Diagnostic of the reducing tensor-memory load (tcgen05.ld.red, sm_103a)
  * with which every attention path takes the row maximum of a full 128-key

@@ -95,7 +95,7 @@ _SIGS = {
     "h3kv_set_wait_timeout_ns": (ctypes.c_int, [ctypes.c_uint64]),
     "h3kv_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _vp]),
     "h3kv_selftest_tmem_ld_max": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), _vp]),
-    "h3kv_attend_launch_count": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]),
+    "h3kv_attend_launch_count": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]),
     "h3kv_debug_withhold_p": (ctypes.c_int, [ctypes.c_int32]),
     "h3kv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
 }

@@ -301,7 +301,7 @@ h3kv_status h3kv_attend(const uint16_t *Q, int64_t q_seq, const h3kv_store *stor
   a.err = d->err;
   a.timeout_ns = g_timeout_ns.load();
   a.withhold_p_tile1 = g_withhold_p_tile1.load();
-  return h3kv::launch_query_chunks(a, q_seq, q_chunk, store->heads, [&](const h3kv::AttnArgs &x, bool overlap) {
+  return h3kv::launch_query_chunks(a, q_seq, store->seq, q_chunk, store->heads, [&](const h3kv::AttnArgs &x, bool overlap) {
     return h3kv::launch_attend_kvi8r(x, overlap, static_cast<cudaStream_t>(stream));
   });
 }
@@ -341,7 +341,7 @@ h3kv_status h3kv_attend_exact(const uint16_t *Q, int64_t q_seq, const uint16_t *
   a.err = d->err;
   a.timeout_ns = g_timeout_ns.load();
   a.withhold_p_tile1 = g_withhold_p_tile1.load();
-  return h3kv::launch_query_chunks(a, q_seq, q_chunk, heads, [&](const h3kv::AttnArgs &x, bool overlap) {
+  return h3kv::launch_query_chunks(a, q_seq, kv_seq, q_chunk, heads, [&](const h3kv::AttnArgs &x, bool overlap) {
     return h3kv::launch_attend_exact(tq, tk, tv, x, overlap, static_cast<cudaStream_t>(stream));
   });
 }
@@ -709,7 +709,7 @@ h3kv_status h3kv_attend_f8(const uint16_t *Q, int64_t q_seq, const h3kv_store_f8
   a.err = d->err;
   a.timeout_ns = g_timeout_ns.load();
   a.withhold_p_tile1 = g_withhold_p_tile1.load();
-  return h3kv::launch_query_chunks(a, q_seq, q_chunk, store->heads, [&](const h3kv::F8Args &x, bool overlap) {
+  return h3kv::launch_query_chunks(a, q_seq, store->seq, q_chunk, store->heads, [&](const h3kv::F8Args &x, bool overlap) {
     return h3kv::launch_attend_f8(tk, tv, x, overlap, static_cast<cudaStream_t>(stream));
   });
 }
@@ -781,13 +781,13 @@ h3kv_status h3kv_attend_fp4(const uint16_t *Q, int64_t q_seq, const h3kv_store_f
   a.err = d->err;
   a.timeout_ns = g_timeout_ns.load();
   a.withhold_p_tile1 = g_withhold_p_tile1.load();
-  return h3kv::launch_query_chunks(a, q_seq, q_chunk, store->heads, [&](const h3kv::AttnArgs &x, bool overlap) {
+  return h3kv::launch_query_chunks(a, q_seq, store->seq, q_chunk, store->heads, [&](const h3kv::AttnArgs &x, bool overlap) {
     return h3kv::launch_attend_fp4(x, overlap, static_cast<cudaStream_t>(stream));
   });
 }
 
-int64_t h3kv_attend_launch_count(int64_t q_seq, int32_t heads, int32_t q_chunk) {
-  return h3kv::launch_count(q_seq, q_chunk, heads);
+int64_t h3kv_attend_launch_count(int64_t q_seq, int64_t kv_seq, int32_t heads, int32_t q_chunk) {
+  return h3kv::launch_count(q_seq, kv_seq, q_chunk, heads);
 }
 
 h3kv_status h3kv_set_wait_timeout_ns(uint64_t timeout_ns) {

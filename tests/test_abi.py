@@ -252,15 +252,17 @@ def test_tmem_selftest_rejects_null_before_device_work():
 
 
 def test_attend_launch_count():
-    # one launch per chunk over all heads below 16 CTAs (256 rows each) per head
-    # and chunk, else heads x chunks launches of one head each
-    assert b.h3kv_attend_launch_count(217088, 32, 16384) == 32 * 14
-    assert b.h3kv_attend_launch_count(217088, 32, 4096) == 32 * 53
-    assert b.h3kv_attend_launch_count(217088, 32, 3841) == 32 * 57   # 16 CTAs per chunk
-    assert b.h3kv_attend_launch_count(217088, 32, 3840) == 57        # 15 CTAs per chunk
-    assert b.h3kv_attend_launch_count(65536, 32, 1024) == 64
-    assert b.h3kv_attend_launch_count(3000, 1, 256) == 12        # one head: chunk by chunk
-    assert b.h3kv_attend_launch_count(1000, 8, 16384) == 1        # 4 CTAs per head: one launch
-    assert b.h3kv_attend_launch_count(8192, 8, 16384) == 8        # 32 CTAs per head: per head
-    assert b.h3kv_attend_launch_count(0, 8, 256) == 0
-    assert b.h3kv_attend_launch_count(100, 8, 0) == 0
+    # head by head (heads x chunks launches) with more than one head, at least
+    # 131072 keys and at least 16 CTAs (256 rows each) per head and chunk;
+    # otherwise one launch per chunk over all heads
+    n = b.h3kv_attend_launch_count
+    assert n(217088, 217088, 32, 16384) == 32 * 14
+    assert n(217088, 217088, 32, 4096) == 32 * 53
+    assert n(217088, 217088, 32, 3841) == 32 * 57   # 16 CTAs per chunk
+    assert n(217088, 217088, 32, 3840) == 57        # 15 CTAs per chunk
+    assert n(217088, 131072, 32, 16384) == 32 * 14  # the shortest head-major key count
+    assert n(217088, 131071, 32, 16384) == 14
+    assert n(65536, 65536, 32, 16384) == 4          # shorter sequences: chunk by chunk
+    assert n(3000, 300000, 1, 256) == 12            # one head: chunk by chunk
+    assert n(0, 217088, 8, 256) == 0
+    assert n(100, 217088, 8, 0) == 0

@@ -125,6 +125,35 @@ def test_kvi8r_sweep_h32_l65536_bit_identical(cuda):
         del base
 
 
+def test_launch_orders_bit_identical(cuda):
+    # 131072 keys: 4500-row (18 CTAs) and 4096-row (16 CTAs) chunks launch head
+    # by head, 3840-row chunks (15 CTAs) one launch per chunk over all heads;
+    # a row's arithmetic is the same in every launch, on all four paths
+    H, L, QS = 3, 131072, 4500
+    b = _b()
+    n = b.h3kv_attend_launch_count
+    assert (n(QS, L, H, 4500), n(QS, L, H, 4096), n(QS, L, H, 3840)) == (3, 6, 2)
+    q, k, v = synth.make_qkv(H, L, seed=13, q_seq=QS, k_outliers=True, device=cuda)
+    st, st8, st4 = b.build_store(k, v), b.build_store_f8(k, v), b.build_store_fp4(k, v)
+    calls = {
+        "kvi8r": lambda c: b.attend(q, st, q_chunk=c, kv_block=16384),
+        "exact": lambda c: b.attend_exact(q, k, v, q_chunk=c, kv_block=16384),
+        "kvf8s": lambda c: b.attend_f8(q, st8, q_chunk=c, kv_block=16384),
+        "kvfp4": lambda c: b.attend_fp4(q, st4, q_chunk=c, kv_block=16384),
+    }
+    for name, call in calls.items():
+        outs = [call(c) for c in (4500, 4096, 3840)]
+        b.sync_status()
+        for o in outs[1:]:
+            assert torch.equal(o, outs[0]), name
+    # and the head-major kvi8r result against the oracle on sampled rows of one head
+    rows = torch.randperm(QS, generator=torch.Generator().manual_seed(5))[:16].sort().values.to(cuda)
+    out = b.attend(q, st, q_chunk=4096, kv_block=16384)
+    b.sync_status()
+    ref = oracle.attend(q[[1]][:, rows].cpu(), oracle_store_heads(k[[1]].cpu(), v[[1]].cpu(), [0]))
+    compare_attention(out[[1]][:, rows], ref, "head-major 3x4500x131072")
+
+
 # ------------------------------------------------------------------ exact --
 @pytest.mark.parametrize("q_chunk,kv_block", [(256, 0), (1024, 512), (1, 128)])
 def test_exact_tiny(cuda, q_chunk, kv_block):
