@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define H3KV_ABI_VERSION 8u
+#define H3KV_ABI_VERSION 9u
 #define H3KV_HEAD_DIM 128
 /* kv_block = 0 on the kvi8r path means this many tokens (the kv_block
  * default of the kv_store row). */
