@@ -22,7 +22,9 @@ def _b():
 @pytest.mark.parametrize("heads,q_seq,kv_seq,q_chunk,kv_block",
                          [(1, 1024, 1024, 256, 512), (2, 1000, 1337, 300, 512), (3, 700, 900, 4096, 0),
                           (1, 5, 300, 1, 128), (3, 4096, 2000, 1000, 1024), (2, 4100, 513, 2048, 256),
-                          (2, 5000, 2000, 256, 512), (1, 1100, 300, 1, 128), (2, 3000, 700, 2048, 256)])
+                          (2, 5000, 2000, 256, 512), (1, 1100, 300, 1, 128), (2, 3000, 700, 2048, 256),
+                          # device attention launches these head by head (131072 keys, 16 CTAs per chunk)
+                          (2, 4500, 131072, 4096, 16384)])
 def test_hostio_bit_identical_to_device_attend(cuda, heads, q_seq, kv_seq, q_chunk, kv_block):
     b = _b()
     q, k, v = synth.make_qkv(heads, kv_seq, seed=31, q_seq=q_seq, k_outliers=True)

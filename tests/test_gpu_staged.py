@@ -51,6 +51,22 @@ def test_staged_bit_identical_to_resident(cuda, heads, q_seq, kv_seq, q_chunk, k
     compare_attention(staged_host, oracle.attend(q, oracle.build_store(k, v)), f"staged {heads}x{q_seq}x{kv_seq}")
 
 
+def test_staged_bit_identical_to_head_major_resident(cuda):
+    # at 131072 keys with 4096-row chunks the resident call launches head by
+    # head; the staged call runs block by block over all heads
+    b = _b()
+    heads, q_seq, kv_seq, q_chunk, kv_block = 2, 4500, 131072, 4096, 16384
+    assert b.h3kv_attend_launch_count(q_seq, kv_seq, heads, q_chunk) == heads * 2
+    q, k, v = synth.make_qkv(heads, kv_seq, seed=33, q_seq=q_seq, k_outliers=True, device=cuda)
+    dev = b.build_store(k, v)
+    host = b.build_store(k, v, out=b.Store.empty(heads, kv_seq, host=True))
+    ref = b.attend(q, dev, q_chunk=q_chunk, kv_block=kv_block)
+    staging = torch.empty(b.staging_bytes_double(heads, kv_block), dtype=torch.uint8, device=cuda)
+    out = b.attend_staged(q, host, q_chunk=q_chunk, kv_block=kv_block, staging=staging)
+    b.sync_status()
+    assert torch.equal(out, ref)
+
+
 def test_staged_reuses_scratch_across_calls(cuda):
     # the same staging buffer and state serve consecutive calls; nothing of a
     # previous call may leak into the next
